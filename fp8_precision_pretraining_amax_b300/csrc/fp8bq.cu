@@ -1,0 +1,263 @@
+// Host side of libfp8bq: argument validation, TMA descriptor encoding and
+// kernel launches behind the C ABI declared in include/fp8bq.h.
+//
+// The whole device code is one translation unit (kernels from quantize.cuh
+// and gemm.cuh), compiled for sm_103a only.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "fp8bq.h"
+#include "gemm.cuh"
+#include "quantize.cuh"
+
+namespace {
+
+// Bit 0: a kernel gave up on a bounded wait.
+__device__ unsigned int g_status_word;
+
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool probed = false;
+    bool supported = false;
+    int sms = 0;
+    unsigned int* status = nullptr;  // device address of g_status_word
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int probe_device(DeviceState** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FP8BQ_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return FP8BQ_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState& d = g_dev[dev];
+    if (!d.probed) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return FP8BQ_ERR_CUDA;
+        d.supported = (major == 10 && minor == 3);
+        d.sms = sms;
+        if (d.supported) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return FP8BQ_ERR_CUDA;
+            d.status = static_cast<unsigned int*>(p);
+            const int smem = static_cast<int>(fp8bq::kGemmSmemBytes);
+            if (cudaFuncSetAttribute(fp8bq::gemm_block_scaled_kernel<fp8bq::kModeFprop>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+                cudaFuncSetAttribute(fp8bq::gemm_block_scaled_kernel<fp8bq::kModeDgrad>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+                cudaFuncSetAttribute(fp8bq::gemm_block_scaled_kernel<fp8bq::kModeWgrad>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+                return FP8BQ_ERR_CUDA;
+            if (g_encode == nullptr) {
+                void* fn = nullptr;
+                cudaDriverEntryPointQueryResult q;
+                if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                        cudaSuccess ||
+                    q != cudaDriverEntryPointSuccess || fn == nullptr)
+                    return FP8BQ_ERR_CUDA;
+                g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+            }
+        }
+        d.probed = true;
+    }
+    if (!d.supported) return FP8BQ_ERR_DEVICE;
+    *out = &d;
+    return FP8BQ_OK;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline int elem_size(int dtype) { return dtype == FP8BQ_BF16 ? 2 : 4; }
+
+inline int launch_status() { return cudaGetLastError() == cudaSuccess ? FP8BQ_OK : FP8BQ_ERR_CUDA; }
+
+// 2-D uint8 tensor [outer][inner] (inner contiguous, pitch == inner), tiles of
+// box_outer x 128 bytes with 128-byte swizzle.  Rows past `outer` read as 0.
+int encode_u8_map(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {inner};
+    const cuuint32_t box[2] = {128, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FP8BQ_OK : FP8BQ_ERR_CUDA;
+}
+
+template <int MODE>
+int run_gemm(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, uint16_t* D, int64_t I,
+             int64_t J, int64_t Kr, cudaStream_t stream) {
+    if (I < 0 || J < 0 || Kr < 0) return FP8BQ_ERR_SHAPE;
+    if ((I % 128) || (J % 128) || (Kr % 128)) return FP8BQ_ERR_SHAPE;
+    if (I >= (int64_t(1) << 31) || J >= (int64_t(1) << 31) || Kr >= (int64_t(1) << 31)) return FP8BQ_ERR_SHAPE;
+    if (I == 0 || J == 0) return FP8BQ_OK;
+    if (D == nullptr) return FP8BQ_ERR_NULL;
+    if (Kr > 0 && (!A || !sA || !B || !sB)) return FP8BQ_ERR_NULL;
+    if (!aligned16(D)) return FP8BQ_ERR_ALIGN;
+    if (Kr > 0 && (!aligned16(A) || !aligned16(B) || !aligned16(sA) || !aligned16(sB))) return FP8BQ_ERR_ALIGN;
+    DeviceState* dev = nullptr;
+    int st = probe_device(&dev);
+    if (st != FP8BQ_OK) return st;
+    if (Kr == 0) {
+        // empty reduction: the product is exactly zero
+        return cudaMemsetAsync(D, 0, static_cast<size_t>(I) * J * 2, stream) == cudaSuccess ? FP8BQ_OK
+                                                                                            : FP8BQ_ERR_CUDA;
+    }
+
+    CUtensorMap ta, tb;
+    if (encode_u8_map(&ta, A, Kr, I, fp8bq::kBM) != FP8BQ_OK) return FP8BQ_ERR_CUDA;
+    if (encode_u8_map(&tb, B, Kr, J, fp8bq::kBN) != FP8BQ_OK) return FP8BQ_ERR_CUDA;
+
+    fp8bq::GemmParams p;
+    p.sA = sA;
+    p.sB = sB;
+    p.D = D;
+    p.I = static_cast<int>(I);
+    p.J = static_cast<int>(J);
+    p.KC = static_cast<int>(Kr / 128);
+    p.tiles_n = static_cast<int>((J + fp8bq::kBN - 1) / fp8bq::kBN);
+    const int64_t tiles = (I / fp8bq::kBM) * p.tiles_n;
+    if (tiles >= (int64_t(1) << 31)) return FP8BQ_ERR_SHAPE;
+    p.num_tiles = static_cast<int>(tiles);
+    p.timeout_ns = kDefaultTimeoutNs;
+    const int grid = static_cast<int>(tiles < dev->sms ? tiles : dev->sms);
+    fp8bq::gemm_block_scaled_kernel<MODE>
+        <<<grid, fp8bq::kGemmThreads, fp8bq::kGemmSmemBytes, stream>>>(ta, tb, p, dev->status);
+    return launch_status();
+}
+
+}  // namespace
+
+extern "C" {
+
+int fp8bq_quantize_rowwise(const void* x, int dtype, int64_t R, int64_t C, int64_t ldx, uint8_t* q, float* s,
+                           fp8bq_stream_t stream) {
+    if (dtype != FP8BQ_BF16 && dtype != FP8BQ_F32) return FP8BQ_ERR_DTYPE;
+    if (R < 0 || C < 0 || ldx < C || (C % 128)) return FP8BQ_ERR_SHAPE;
+    if (R == 0 || C == 0) return FP8BQ_OK;
+    if (!x || !q || !s) return FP8BQ_ERR_NULL;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(s) || ((ldx * elem_size(dtype)) % 16)) return FP8BQ_ERR_ALIGN;
+    DeviceState* dev = nullptr;
+    int st = probe_device(&dev);
+    if (st != FP8BQ_OK) return st;
+    const int64_t tiles = R * (C / 128);
+    const int64_t blocks = (tiles + 31) / 32;  // 8 warps x 4 tiles
+    if (blocks >= (int64_t(1) << 31)) return FP8BQ_ERR_SHAPE;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if (dtype == FP8BQ_BF16)
+        fp8bq::quantize_rowwise_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, cs>>>(x, R, C, ldx, q, s);
+    else
+        fp8bq::quantize_rowwise_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, cs>>>(x, R, C, ldx, q, s);
+    return launch_status();
+}
+
+int fp8bq_quantize_colwise(const void* x, int dtype, int64_t M, int64_t C, int64_t ldx, uint8_t* qT, float* s,
+                           fp8bq_stream_t stream) {
+    if (dtype != FP8BQ_BF16 && dtype != FP8BQ_F32) return FP8BQ_ERR_DTYPE;
+    if (M < 0 || C < 0 || ldx < C || (M % 128) || (C % 8)) return FP8BQ_ERR_SHAPE;
+    if (M == 0 || C == 0) return FP8BQ_OK;
+    if (!x || !qT || !s) return FP8BQ_ERR_NULL;
+    if (!aligned16(x) || !aligned16(qT) || !aligned16(s) || ((ldx * elem_size(dtype)) % 16)) return FP8BQ_ERR_ALIGN;
+    if (M / 128 > 65535) return FP8BQ_ERR_SHAPE;
+    DeviceState* dev = nullptr;
+    int st = probe_device(&dev);
+    if (st != FP8BQ_OK) return st;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const int cw = dtype == FP8BQ_BF16 ? 128 : 64;
+    dim3 grid(static_cast<unsigned>((C + cw - 1) / cw), static_cast<unsigned>(M / 128));
+    if (dtype == FP8BQ_BF16)
+        fp8bq::quantize_colwise_kernel<false><<<grid, 256, 0, cs>>>(x, M, C, ldx, qT, s);
+    else
+        fp8bq::quantize_colwise_kernel<true><<<grid, 256, 0, cs>>>(x, M, C, ldx, qT, s);
+    return launch_status();
+}
+
+int fp8bq_quantize_weight_block(const void* w, int dtype, int64_t N, int64_t K, int64_t ldw, uint8_t* q,
+                                uint8_t* qT, float* s, fp8bq_stream_t stream) {
+    if (dtype != FP8BQ_BF16 && dtype != FP8BQ_F32) return FP8BQ_ERR_DTYPE;
+    if (N < 0 || K < 0 || ldw < K || (N % 128) || (K % 128)) return FP8BQ_ERR_SHAPE;
+    if (N == 0 || K == 0) return FP8BQ_OK;
+    if (!w || !q || !s) return FP8BQ_ERR_NULL;
+    if (!aligned16(w) || !aligned16(q) || !aligned16(s) || (qT && !aligned16(qT)) ||
+        ((ldw * elem_size(dtype)) % 16))
+        return FP8BQ_ERR_ALIGN;
+    if (N / 128 > 65535 || K / 128 >= (int64_t(1) << 31)) return FP8BQ_ERR_SHAPE;
+    DeviceState* dev = nullptr;
+    int st = probe_device(&dev);
+    if (st != FP8BQ_OK) return st;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>(N / 128));
+    if (dtype == FP8BQ_BF16)
+        fp8bq::quantize_weight_block_kernel<false><<<grid, 256, 0, cs>>>(w, N, K, ldw, q, qT, s);
+    else
+        fp8bq::quantize_weight_block_kernel<true><<<grid, 256, 0, cs>>>(w, N, K, ldw, q, qT, s);
+    return launch_status();
+}
+
+int fp8bq_gemm_fprop(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw, uint16_t* y, int64_t M,
+                     int64_t N, int64_t K, fp8bq_stream_t stream) {
+    return run_gemm<fp8bq::kModeFprop>(xq, sx, wq, sw, y, M, N, K, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fp8bq_gemm_dgrad(const uint8_t* dyq, const float* sdy, const uint8_t* wqT, const float* sw, uint16_t* dx,
+                     int64_t M, int64_t N, int64_t K, fp8bq_stream_t stream) {
+    return run_gemm<fp8bq::kModeDgrad>(dyq, sdy, wqT, sw, dx, M, K, N, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fp8bq_gemm_wgrad(const uint8_t* dyqT, const float* sdyT, const uint8_t* xqT, const float* sxT, uint16_t* dw,
+                     int64_t M, int64_t N, int64_t K, fp8bq_stream_t stream) {
+    return run_gemm<fp8bq::kModeWgrad>(dyqT, sdyT, xqT, sxT, dw, N, K, M, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fp8bq_check(fp8bq_stream_t stream) {
+    DeviceState* dev = nullptr;
+    int st = probe_device(&dev);
+    if (st != FP8BQ_OK) return st;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    unsigned int word = 0;
+    if (cudaStreamSynchronize(cs) != cudaSuccess) return FP8BQ_ERR_CUDA;
+    if (cudaMemcpyAsync(&word, dev->status, sizeof(word), cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+        return FP8BQ_ERR_CUDA;
+    if (cudaMemsetAsync(dev->status, 0, sizeof(word), cs) != cudaSuccess) return FP8BQ_ERR_CUDA;
+    if (cudaStreamSynchronize(cs) != cudaSuccess) return FP8BQ_ERR_CUDA;
+    return (word & 1u) ? FP8BQ_ERR_TIMEOUT : FP8BQ_OK;
+}
+
+const char* fp8bq_status_string(int status) {
+    switch (status) {
+        case FP8BQ_OK: return "ok";
+        case FP8BQ_ERR_NULL: return "null pointer argument";
+        case FP8BQ_ERR_SHAPE: return "invalid shape (negative, not a multiple of 128, or pitch < width)";
+        case FP8BQ_ERR_ALIGN: return "pointer or row pitch not 16-byte aligned";
+        case FP8BQ_ERR_DTYPE: return "unknown input dtype";
+        case FP8BQ_ERR_DEVICE: return "current device is not an sm_103 GPU";
+        case FP8BQ_ERR_CUDA: return "CUDA call or kernel launch failed";
+        case FP8BQ_ERR_TIMEOUT: return "a kernel gave up waiting on its pipeline (outputs undefined)";
+        default: return "unknown status";
+    }
+}
+
+int fp8bq_selftest_wait_timeout(int64_t limit_ns, fp8bq_stream_t stream) {
+    DeviceState* dev = nullptr;
+    int st = probe_device(&dev);
+    if (st != FP8BQ_OK) return st;
+    if (limit_ns < 1000) limit_ns = 1000;
+    if (limit_ns > 2000000000ll) limit_ns = 2000000000ll;
+    fp8bq::wait_timeout_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<uint64_t>(limit_ns), dev->status);
+    return launch_status();
+}
+
+}  // extern "C"

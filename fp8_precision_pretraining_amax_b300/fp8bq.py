@@ -1,0 +1,262 @@
+"""Python binding of libfp8bq (block-scaled FP8 linear layer for B300).
+
+Argument marshalling only: every function passes torch tensors' device
+pointers, sizes and the current CUDA stream to the C ABI of include/fp8bq.h
+and raises on a non-OK status.  All arithmetic runs in the library's CUDA
+kernels; there is no CPU or library fallback.  Importing this module fails
+loudly when libfp8bq.so has not been built.
+
+Functions carry the C names (fp8bq_quantize_rowwise, ...) and take every
+buffer explicitly; the unprefixed forms (quantize_rowwise, gemm_fprop, ...)
+allocate the outputs with torch and return them.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfp8bq.so")
+
+OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_DTYPE, ERR_DEVICE, ERR_CUDA, ERR_TIMEOUT = range(8)
+BF16, F32 = 0, 1
+
+#: Names of the C-ABI entry points declared in include/fp8bq.h.
+C_FUNCTIONS = (
+    "fp8bq_quantize_rowwise", "fp8bq_quantize_colwise", "fp8bq_quantize_weight_block",
+    "fp8bq_gemm_fprop", "fp8bq_gemm_dgrad", "fp8bq_gemm_wgrad",
+    "fp8bq_check", "fp8bq_status_string", "fp8bq_selftest_wait_timeout",
+)
+
+
+def _load():
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(
+            f"libfp8bq.so is not built ({_LIB_PATH}); run "
+            "`python -m fp8_precision_pretraining_amax_b300.build` (needs nvcc with sm_103a)")
+    lib = ctypes.CDLL(_LIB_PATH)
+    vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    sig = {
+        "fp8bq_quantize_rowwise": [vp, i32, i64, i64, i64, vp, vp, vp],
+        "fp8bq_quantize_colwise": [vp, i32, i64, i64, i64, vp, vp, vp],
+        "fp8bq_quantize_weight_block": [vp, i32, i64, i64, i64, vp, vp, vp, vp],
+        "fp8bq_gemm_fprop": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
+        "fp8bq_gemm_dgrad": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
+        "fp8bq_gemm_wgrad": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
+        "fp8bq_check": [vp],
+        "fp8bq_selftest_wait_timeout": [i64, vp],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = i32
+    lib.fp8bq_status_string.argtypes = [i32]
+    lib.fp8bq_status_string.restype = ctypes.c_char_p
+    return lib
+
+
+lib = _load()
+
+
+class Fp8bqError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+def status_string(status: int) -> str:
+    return lib.fp8bq_status_string(int(status)).decode()
+
+
+def _raise(status: int, where: str) -> None:
+    if status != OK:
+        raise Fp8bqError(status, where)
+
+
+def _stream(t: Optional[torch.Tensor] = None) -> int:
+    dev = t.device if t is not None and t.is_cuda else None
+    return torch.cuda.current_stream(dev).cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"input must be bfloat16 or float32, got {t.dtype}")
+
+
+def _need(t: torch.Tensor, dtype, shape, name: str) -> None:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _rows_input(x: torch.Tensor, name: str) -> int:
+    if x.dim() != 2 or not x.is_cuda:
+        raise ValueError(f"{name} must be a 2-D CUDA tensor")
+    if x.stride(1) != 1:
+        raise ValueError(f"{name} must have unit inner stride")
+    return x.stride(0) if x.shape[0] > 1 else x.shape[1]
+
+
+# ---------------------------------------------------------------------------
+# C-named entry points (caller supplies every buffer)
+# ---------------------------------------------------------------------------
+
+def fp8bq_quantize_rowwise(x: torch.Tensor, q: torch.Tensor, s: torch.Tensor) -> None:
+    """x [R, C] bf16/f32 -> q [R, C] uint8 codes, s [C/128, R] f32 scales."""
+    ldx = _rows_input(x, "x")
+    R, C = x.shape
+    _need(q, torch.uint8, (R, C), "q")
+    _need(s, torch.float32, (C // 128, R), "s")
+    with torch.cuda.device(x.device):
+        _raise(lib.fp8bq_quantize_rowwise(_ptr(x), _dtype_code(x), R, C, ldx, _ptr(q), _ptr(s), _stream(x)),
+               "fp8bq_quantize_rowwise")
+
+
+def fp8bq_quantize_colwise(x: torch.Tensor, qT: torch.Tensor, s: torch.Tensor) -> None:
+    """x [M, C] bf16/f32 -> qT [C, M] uint8 codes (128x1 tiles), s [M/128, C] f32."""
+    ldx = _rows_input(x, "x")
+    M, C = x.shape
+    _need(qT, torch.uint8, (C, M), "qT")
+    _need(s, torch.float32, (M // 128, C), "s")
+    with torch.cuda.device(x.device):
+        _raise(lib.fp8bq_quantize_colwise(_ptr(x), _dtype_code(x), M, C, ldx, _ptr(qT), _ptr(s), _stream(x)),
+               "fp8bq_quantize_colwise")
+
+
+def fp8bq_quantize_weight_block(w: torch.Tensor, q: torch.Tensor, qT: Optional[torch.Tensor],
+                                s: torch.Tensor) -> None:
+    """w [N, K] -> q [N, K], qT [K, N] (or None), s [N/128, K/128]."""
+    ldw = _rows_input(w, "w")
+    N, K = w.shape
+    _need(q, torch.uint8, (N, K), "q")
+    if qT is not None:
+        _need(qT, torch.uint8, (K, N), "qT")
+    _need(s, torch.float32, (N // 128, K // 128), "s")
+    with torch.cuda.device(w.device):
+        _raise(lib.fp8bq_quantize_weight_block(_ptr(w), _dtype_code(w), N, K, ldw, _ptr(q), _ptr(qT), _ptr(s),
+                                               _stream(w)), "fp8bq_quantize_weight_block")
+
+
+def fp8bq_gemm_fprop(xq, sx, wq, sw, y) -> None:
+    """Y [M, N] bf16 = Xq Wq^T with per-chunk scales sx [K/128, M], sw [N/128, K/128]."""
+    M, K = xq.shape
+    N = wq.shape[0]
+    _need(xq, torch.uint8, (M, K), "xq")
+    _need(sx, torch.float32, (K // 128, M), "sx")
+    _need(wq, torch.uint8, (N, K), "wq")
+    _need(sw, torch.float32, (N // 128, K // 128), "sw")
+    _need(y, torch.bfloat16, (M, N), "y")
+    with torch.cuda.device(y.device):
+        _raise(lib.fp8bq_gemm_fprop(_ptr(xq), _ptr(sx), _ptr(wq), _ptr(sw), _ptr(y), M, N, K, _stream(y)),
+               "fp8bq_gemm_fprop")
+
+
+def fp8bq_gemm_dgrad(dyq, sdy, wqT, sw, dx) -> None:
+    """dX [M, K] bf16 = dYq Wq with dyq [M, N], sdy [N/128, M], wqT [K, N], sw [N/128, K/128]."""
+    M, N = dyq.shape
+    K = wqT.shape[0]
+    _need(dyq, torch.uint8, (M, N), "dyq")
+    _need(sdy, torch.float32, (N // 128, M), "sdy")
+    _need(wqT, torch.uint8, (K, N), "wqT")
+    _need(sw, torch.float32, (N // 128, K // 128), "sw")
+    _need(dx, torch.bfloat16, (M, K), "dx")
+    with torch.cuda.device(dx.device):
+        _raise(lib.fp8bq_gemm_dgrad(_ptr(dyq), _ptr(sdy), _ptr(wqT), _ptr(sw), _ptr(dx), M, N, K, _stream(dx)),
+               "fp8bq_gemm_dgrad")
+
+
+def fp8bq_gemm_wgrad(dyqT, sdyT, xqT, sxT, dw) -> None:
+    """dW [N, K] bf16 = dY^T X over tokens: dyqT [N, M], sdyT [M/128, N], xqT [K, M], sxT [M/128, K]."""
+    N, M = dyqT.shape
+    K = xqT.shape[0]
+    _need(dyqT, torch.uint8, (N, M), "dyqT")
+    _need(sdyT, torch.float32, (M // 128, N), "sdyT")
+    _need(xqT, torch.uint8, (K, M), "xqT")
+    _need(sxT, torch.float32, (M // 128, K), "sxT")
+    _need(dw, torch.bfloat16, (N, K), "dw")
+    with torch.cuda.device(dw.device):
+        _raise(lib.fp8bq_gemm_wgrad(_ptr(dyqT), _ptr(sdyT), _ptr(xqT), _ptr(sxT), _ptr(dw), M, N, K, _stream(dw)),
+               "fp8bq_gemm_wgrad")
+
+
+def fp8bq_check(device=None) -> None:
+    """Synchronize the current stream and raise if a kernel reported a device-side timeout."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        _raise(lib.fp8bq_check(torch.cuda.current_stream(dev).cuda_stream), "fp8bq_check")
+
+
+def fp8bq_selftest_wait_timeout(limit_ns: int, device=None) -> None:
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        _raise(lib.fp8bq_selftest_wait_timeout(int(limit_ns), torch.cuda.current_stream(dev).cuda_stream),
+               "fp8bq_selftest_wait_timeout")
+
+
+def fp8bq_status_string(status: int) -> str:
+    return status_string(status)
+
+
+# ---------------------------------------------------------------------------
+# Allocating forms
+# ---------------------------------------------------------------------------
+
+def quantize_rowwise(x: torch.Tensor) -> Tuple[torch.Tensor, torch.Tensor]:
+    R, C = x.shape
+    q = torch.empty((R, C), dtype=torch.uint8, device=x.device)
+    s = torch.empty((C // 128, R), dtype=torch.float32, device=x.device)
+    fp8bq_quantize_rowwise(x, q, s)
+    return q, s
+
+
+def quantize_colwise(x: torch.Tensor) -> Tuple[torch.Tensor, torch.Tensor]:
+    M, C = x.shape
+    qT = torch.empty((C, M), dtype=torch.uint8, device=x.device)
+    s = torch.empty((M // 128, C), dtype=torch.float32, device=x.device)
+    fp8bq_quantize_colwise(x, qT, s)
+    return qT, s
+
+
+def quantize_weight_block(w: torch.Tensor, transpose: bool = True):
+    N, K = w.shape
+    q = torch.empty((N, K), dtype=torch.uint8, device=w.device)
+    qT = torch.empty((K, N), dtype=torch.uint8, device=w.device) if transpose else None
+    s = torch.empty((N // 128, K // 128), dtype=torch.float32, device=w.device)
+    fp8bq_quantize_weight_block(w, q, qT, s)
+    return q, qT, s
+
+
+def gemm_fprop(xq, sx, wq, sw) -> torch.Tensor:
+    y = torch.empty((xq.shape[0], wq.shape[0]), dtype=torch.bfloat16, device=xq.device)
+    fp8bq_gemm_fprop(xq, sx, wq, sw, y)
+    return y
+
+
+def gemm_dgrad(dyq, sdy, wqT, sw) -> torch.Tensor:
+    dx = torch.empty((dyq.shape[0], wqT.shape[0]), dtype=torch.bfloat16, device=dyq.device)
+    fp8bq_gemm_dgrad(dyq, sdy, wqT, sw, dx)
+    return dx
+
+
+def gemm_wgrad(dyqT, sdyT, xqT, sxT) -> torch.Tensor:
+    dw = torch.empty((dyqT.shape[0], xqT.shape[0]), dtype=torch.bfloat16, device=dyqT.device)
+    fp8bq_gemm_wgrad(dyqT, sdyT, xqT, sxT, dw)
+    return dw
+
+
+check = fp8bq_check
+selftest_wait_timeout = fp8bq_selftest_wait_timeout

@@ -1,0 +1,65 @@
+"""One nn.Linear on the block-scaled FP8 path: Fprop, Dgrad and Wgrad.
+
+The Puro-2B report (section 2, "FP8") runs the matrix multiplications of the
+main linear layers in FP8 with DeepSeek-V3-style fine-grained quantization and
+keeps everything else in BF16/FP32.  For a layer with input X [M, K], weight
+W [N, K] and output gradient dY [M, N] one training step does:
+
+  forward    X -> row-wise 1x128 codes   W -> 128x128 block codes (+ transposed)
+             Y  = Fprop(Xq, Wq)                                         [M, N]
+  backward   dY -> row-wise 1x128 codes  dX = Dgrad(dYq, Wq^T)          [M, K]
+             dY, X -> column-wise 128x1 codes (transposed)
+             dW = Wgrad(dYq^T, Xq^T)                                    [N, K]
+
+`LinearFP8` owns the code/scale buffers for one shape so that a step performs
+no allocation; every call is a C-ABI launch on the current stream.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import fp8bq
+
+
+class LinearFP8:
+    """Pre-allocated workspace for one linear layer of shape (M, K) -> N."""
+
+    def __init__(self, M: int, K: int, N: int, device="cuda"):
+        self.M, self.K, self.N = M, K, N
+        u8, f32, bf = torch.uint8, torch.float32, torch.bfloat16
+        e = lambda *shape, dt: torch.empty(shape, dtype=dt, device=device)
+        # forward
+        self.xq, self.sx = e(M, K, dt=u8), e(K // 128, M, dt=f32)
+        self.wq, self.wqT, self.sw = e(N, K, dt=u8), e(K, N, dt=u8), e(N // 128, K // 128, dt=f32)
+        # backward
+        self.dyq, self.sdy = e(M, N, dt=u8), e(N // 128, M, dt=f32)
+        self.dyqT, self.sdyT = e(N, M, dt=u8), e(M // 128, N, dt=f32)
+        self.xqT, self.sxT = e(K, M, dt=u8), e(M // 128, K, dt=f32)
+        self.y, self.dx, self.dw = e(M, N, dt=bf), e(M, K, dt=bf), e(N, K, dt=bf)
+
+    @property
+    def flops_per_gemm(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+    def forward(self, x: torch.Tensor, w: torch.Tensor) -> torch.Tensor:
+        fp8bq.fp8bq_quantize_weight_block(w, self.wq, self.wqT, self.sw)
+        fp8bq.fp8bq_quantize_rowwise(x, self.xq, self.sx)
+        fp8bq.fp8bq_gemm_fprop(self.xq, self.sx, self.wq, self.sw, self.y)
+        return self.y
+
+    def backward(self, x: torch.Tensor, dy: torch.Tensor):
+        """Needs forward() to have quantized the weight (wqT, sw are reused)."""
+        fp8bq.fp8bq_quantize_rowwise(dy, self.dyq, self.sdy)
+        fp8bq.fp8bq_gemm_dgrad(self.dyq, self.sdy, self.wqT, self.sw, self.dx)
+        fp8bq.fp8bq_quantize_colwise(dy, self.dyqT, self.sdyT)
+        fp8bq.fp8bq_quantize_colwise(x, self.xqT, self.sxT)
+        fp8bq.fp8bq_gemm_wgrad(self.dyqT, self.sdyT, self.xqT, self.sxT, self.dw)
+        return self.dx, self.dw
+
+    def step(self, x: torch.Tensor, w: torch.Tensor, dy: torch.Tensor):
+        """Fprop + Dgrad + Wgrad: 3 GEMMs and 5 quantizer launches."""
+        self.forward(x, w)
+        self.backward(x, dy)
+        return self.y, self.dx, self.dw
+
+    LAUNCHES_PER_STEP = 8

@@ -1,0 +1,164 @@
+/*
+ * fp8bq.h — C ABI of the block-scaled FP8 linear layer for B300 (sm_103a).
+ *
+ * What the library computes.  The Puro-2B technical report (section 2, "FP8")
+ * moves the matrix multiplications of the main linear layers onto an FP8
+ * path using DeepSeek-V3's fine-grained block quantization, and keeps
+ * numerically sensitive work in BF16/FP32.  This library is that path for one
+ * nn.Linear with input X [M, K], weight W [N, K] and output gradient dY [M, N]:
+ *
+ *   quantize   activations and gradients per 1x128 tile, weights per 128x128
+ *              block, to E4M3 (OCP FP8) with an FP32 scale per tile:
+ *              s = amax / 448 (s = 1 when amax == 0), code = E4M3 of the
+ *              correctly rounded FP32 quotient x / s, round half to even,
+ *              saturating at +-448.
+ *   GEMM       Fprop  Y  = X  W^T  (reduce over K),
+ *              Dgrad  dX = dY W    (reduce over N),
+ *              Wgrad  dW = dY^T X  (reduce over the M tokens);
+ *              FP8 x FP8 products accumulate in FP32 per 128-wide reduction
+ *              chunk, each chunk is multiplied by the product of its two
+ *              scales and added into an FP32 accumulator, and the result is
+ *              written as BF16 (round half to even).
+ *
+ * Conventions shared by every entry point
+ *   - All pointers except `stream` are DEVICE pointers to memory the caller
+ *     owns.  The library never allocates, frees or retains caller buffers.
+ *   - Matrices are row-major with unit inner stride.  `ld*` arguments are row
+ *     pitches in ELEMENTS of the input type; outputs are dense (pitch = width).
+ *   - Scale arrays are FP32 and chunk-major: the scale of the tile that covers
+ *     row r in reduction chunk c is at s[c * rows + r].  Weight scales are
+ *     sw[N/128][K/128].
+ *   - Every dimension that is quantized or reduced over must be a multiple of
+ *     128; partial tiles are rejected (FP8BQ_ERR_SHAPE).  A zero dimension is
+ *     a no-op that returns FP8BQ_OK (a GEMM with an empty reduction writes
+ *     zeros).
+ *   - Pointers must be 16-byte aligned and row pitches a multiple of 16 bytes
+ *     (TMA and 128-bit vector access), else FP8BQ_ERR_ALIGN.  Inputs and
+ *     outputs must not overlap.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream) and on the calling thread's current device, which must
+ *     be an sm_103 GPU (else FP8BQ_ERR_DEVICE).  Argument errors are detected
+ *     on the host before anything is launched and leave every buffer
+ *     untouched.  A failed launch returns FP8BQ_ERR_CUDA.  Device-side faults
+ *     the kernels detect themselves (a pipeline wait that ran out of time)
+ *     are recorded in a per-device status word and reported by fp8bq_check.
+ *   - The library is thread-safe; it keeps only a per-device status word and
+ *     a cache of device properties, both created on first use.
+ */
+#ifndef FP8BQ_H
+#define FP8BQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same representation as cudaStream_t, without requiring CUDA headers. */
+typedef struct CUstream_st* fp8bq_stream_t;
+
+typedef enum {
+    FP8BQ_OK = 0,
+    FP8BQ_ERR_NULL = 1,     /* a required pointer is NULL                        */
+    FP8BQ_ERR_SHAPE = 2,    /* negative size, non-multiple of 128, pitch < width */
+    FP8BQ_ERR_ALIGN = 3,    /* pointer or pitch not 16-byte aligned              */
+    FP8BQ_ERR_DTYPE = 4,    /* unknown fp8bq_dtype                               */
+    FP8BQ_ERR_DEVICE = 5,   /* current device is not sm_103                      */
+    FP8BQ_ERR_CUDA = 6,     /* a CUDA runtime/driver call or launch failed       */
+    FP8BQ_ERR_TIMEOUT = 7   /* a kernel gave up waiting (reported by fp8bq_check)*/
+} fp8bq_status;
+
+typedef enum {
+    FP8BQ_BF16 = 0,         /* 16-bit bfloat16 input */
+    FP8BQ_F32 = 1           /* 32-bit IEEE float input */
+} fp8bq_dtype;
+
+/*
+ * Row-wise 1x128 quantization (Fprop activations X, Dgrad output gradients dY).
+ *   x      [R][C] input of `dtype`, row pitch ldx elements (ldx >= C)
+ *   q      [R][C] E4M3 codes, dense
+ *   s      [C/128][R] FP32 scales: s[t*R + r] belongs to x[r][128t .. 128t+127]
+ * Requires C % 128 == 0.
+ */
+int fp8bq_quantize_rowwise(const void* x, int dtype, int64_t R, int64_t C, int64_t ldx,
+                           uint8_t* q, float* s, fp8bq_stream_t stream);
+
+/*
+ * Column-wise 128x1 quantization emitted transposed (Wgrad operands: dY and
+ * X quantized along the token dimension that Wgrad reduces over).
+ *   x      [M][C] input of `dtype`, row pitch ldx elements (ldx >= C)
+ *   qT     [C][M] E4M3 codes: qT[c*M + m] is the code of x[m][c], dense
+ *   s      [M/128][C] FP32 scales: s[b*C + c] belongs to x[128b .. 128b+127][c]
+ * Requires M % 128 == 0 and C % 8 == 0 (16-byte rows of BF16).
+ */
+int fp8bq_quantize_colwise(const void* x, int dtype, int64_t M, int64_t C, int64_t ldx,
+                           uint8_t* qT, float* s, fp8bq_stream_t stream);
+
+/*
+ * Weight quantization per 128x128 block.
+ *   w      [N][K] weight of `dtype` (nn.Linear layout), row pitch ldw elements
+ *   q      [N][K] E4M3 codes (Fprop operand), dense
+ *   qT     [K][N] the same codes transposed (Dgrad operand), or NULL to skip
+ *   s      [N/128][K/128] FP32 block scales
+ * Requires N % 128 == 0 and K % 128 == 0.
+ */
+int fp8bq_quantize_weight_block(const void* w, int dtype, int64_t N, int64_t K, int64_t ldw,
+                                uint8_t* q, uint8_t* qT, float* s, fp8bq_stream_t stream);
+
+/*
+ * Fprop: Y[m][n] = sum_c sx[c][m] * sw[n/128][c] * sum_{k in chunk c} D(xq[m][k]) D(wq[n][k])
+ *   xq [M][K] codes, sx [K/128][M]    (from fp8bq_quantize_rowwise of X)
+ *   wq [N][K] codes, sw [N/128][K/128] (from fp8bq_quantize_weight_block of W)
+ *   y  [M][N] BF16 output (16-bit patterns), dense
+ * Requires M, N, K % 128 == 0.
+ */
+int fp8bq_gemm_fprop(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw,
+                     uint16_t* y, int64_t M, int64_t N, int64_t K, fp8bq_stream_t stream);
+
+/*
+ * Dgrad: dX[m][k] = sum_c sdy[c][m] * sw[c][k/128] * sum_{n in chunk c} D(dyq[m][n]) D(wq[n][k])
+ *   dyq [M][N] codes, sdy [N/128][M]   (from fp8bq_quantize_rowwise of dY)
+ *   wqT [K][N] codes (the qT output of fp8bq_quantize_weight_block),
+ *   sw  [N/128][K/128] the weight's block scales
+ *   dx  [M][K] BF16 output, dense
+ * Requires M, N, K % 128 == 0.
+ */
+int fp8bq_gemm_dgrad(const uint8_t* dyq, const float* sdy, const uint8_t* wqT, const float* sw,
+                     uint16_t* dx, int64_t M, int64_t N, int64_t K, fp8bq_stream_t stream);
+
+/*
+ * Wgrad: dW[n][k] = sum_c sdyT[c][n] * sxT[c][k] * sum_{m in chunk c} D(dyqT[n][m]) D(xqT[k][m])
+ *   dyqT [N][M] codes, sdyT [M/128][N] (from fp8bq_quantize_colwise of dY)
+ *   xqT  [K][M] codes, sxT  [M/128][K] (from fp8bq_quantize_colwise of X)
+ *   dw   [N][K] BF16 output, dense
+ * Requires M, N, K % 128 == 0.
+ */
+int fp8bq_gemm_wgrad(const uint8_t* dyqT, const float* sdyT, const uint8_t* xqT, const float* sxT,
+                     uint16_t* dw, int64_t M, int64_t N, int64_t K, fp8bq_stream_t stream);
+
+/*
+ * Synchronize `stream`, then read and clear the current device's status word.
+ * Returns FP8BQ_OK, FP8BQ_ERR_TIMEOUT if a kernel launched since the last
+ * check gave up on a pipeline wait (its outputs are then undefined), or
+ * FP8BQ_ERR_CUDA if the synchronization itself failed.
+ */
+int fp8bq_check(fp8bq_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char* fp8bq_status_string(int status);
+
+/*
+ * Self-test of the bounded-wait path: launches one CTA that waits on a
+ * shared-memory barrier nothing will ever complete, gives up after
+ * `limit_ns` nanoseconds (clamped to [1000, 2e9]) and records
+ * FP8BQ_ERR_TIMEOUT in the status word, exactly as a stalled GEMM pipeline
+ * would.  Lets a caller verify, without faulting or hanging the GPU, that
+ * fp8bq_check reports device-side timeouts.  Returns the launch status.
+ */
+int fp8bq_selftest_wait_timeout(int64_t limit_ns, fp8bq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8BQ_H */

@@ -1,0 +1,103 @@
+"""The C-ABI library builds, loads without a GPU, exports every entry point
+declared in include/fp8bq.h, and rejects bad arguments on the host before it
+touches CUDA (these paths need no device)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from fp8_precision_pretraining_amax_b300 import build as fbuild
+
+HEADER = os.path.join(fbuild.ROOT, "include", "fp8bq.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fp8bq_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = fbuild.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_layer_api():
+    names = _declared_functions()
+    for n in ("fp8bq_quantize_rowwise", "fp8bq_quantize_colwise", "fp8bq_quantize_weight_block",
+              "fp8bq_gemm_fprop", "fp8bq_gemm_dgrad", "fp8bq_gemm_wgrad", "fp8bq_check"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_binding_covers_every_declared_symbol(lib):
+    from fp8_precision_pretraining_amax_b300 import fp8bq
+    assert sorted(fp8bq.C_FUNCTIONS) == _declared_functions()
+    for name in fp8bq.C_FUNCTIONS:
+        assert callable(getattr(fp8bq, name))
+
+
+def test_status_strings(lib):
+    lib.fp8bq_status_string.restype = ctypes.c_char_p
+    for code in range(8):
+        s = lib.fp8bq_status_string(code)
+        assert s and s != b"unknown status"
+    assert lib.fp8bq_status_string(99) == b"unknown status"
+
+
+OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_DTYPE = 0, 1, 2, 3, 4
+P = 0x10000  # a 16-byte-aligned fake device address (never dereferenced)
+
+
+def test_quantizer_argument_errors_are_host_side(lib):
+    f = lib.fp8bq_quantize_rowwise
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    assert f(P, 7, 128, 128, 128, P, P, None) == ERR_DTYPE
+    assert f(P, 0, 128, 100, 128, P, P, None) == ERR_SHAPE        # ragged tile
+    assert f(P, 0, -1, 128, 128, P, P, None) == ERR_SHAPE
+    assert f(P, 0, 4, 256, 128, P, P, None) == ERR_SHAPE          # pitch < width
+    assert f(P, 0, 0, 128, 128, None, None, None) == OK           # empty: no-op
+    assert f(P, 0, 4, 0, 0, None, None, None) == OK
+    assert f(None, 0, 4, 128, 128, P, P, None) == ERR_NULL
+    assert f(P + 2, 0, 4, 128, 128, P, P, None) == ERR_ALIGN
+    assert f(P, 0, 4, 128, 132, P, P, None) == ERR_ALIGN          # 264-byte pitch
+    g = lib.fp8bq_quantize_colwise
+    g.restype = ctypes.c_int
+    g.argtypes = f.argtypes
+    assert g(P, 0, 100, 128, 128, P, P, None) == ERR_SHAPE         # M not a multiple of 128
+    assert g(P, 0, 128, 12, 16, P, P, None) == ERR_SHAPE           # C not a multiple of 8
+    assert g(P, 0, 128, 128, 128, P, None, P) == ERR_NULL
+    h = lib.fp8bq_quantize_weight_block
+    h.restype = ctypes.c_int
+    h.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    assert h(P, 0, 128, 192, 192, P, P, P, None) == ERR_SHAPE
+    assert h(P, 0, 128, 128, 128, P, P + 8, P, None) == ERR_ALIGN
+    assert h(P, 2, 128, 128, 128, P, P, P, None) == ERR_DTYPE
+
+
+def test_gemm_argument_errors_are_host_side(lib):
+    # (M, N, K) with an empty OUTPUT dimension: a host-side no-op.  (An empty
+    # reduction dimension is not: it writes zeros on the device.)
+    empty_out = {"fp8bq_gemm_fprop": (0, 128, 128), "fp8bq_gemm_dgrad": (0, 128, 128),
+                 "fp8bq_gemm_wgrad": (128, 0, 128)}
+    for name in ("fp8bq_gemm_fprop", "fp8bq_gemm_dgrad", "fp8bq_gemm_wgrad"):
+        f = getattr(lib, name)
+        f.restype = ctypes.c_int
+        f.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int64] * 3 + [ctypes.c_void_p]
+        assert f(P, P, P, P, P, 128, 128, 100, None) == ERR_SHAPE
+        assert f(P, P, P, P, P, 128, 192, 128, None) == ERR_SHAPE
+        assert f(P, P, P, P, P, -128, 128, 128, None) == ERR_SHAPE
+        assert f(P, P, P, P, P, *empty_out[name], None) == OK
+        assert f(P, P, P, P, None, 128, 128, 128, None) == ERR_NULL
+        assert f(None, P, P, P, P, 128, 128, 128, None) == ERR_NULL
+        assert f(P, P, P + 4, P, P, 128, 128, 128, None) == ERR_ALIGN
+        assert f(P, P, P, P, P + 2, 128, 128, 128, None) == ERR_ALIGN

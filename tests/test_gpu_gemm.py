@@ -1,0 +1,180 @@
+"""GPU parity of the block-scaled GEMMs with the binary64 oracle.
+
+Inputs to both sides are the same codes and scales, produced on the host by
+the oracle's quantizers or drawn directly as random codes/scales (the GEMM
+accepts any).  Acceptance per element: |C - C_exact| <= 2e-3 * sum_k |a_k b_k|
++ 1 BF16 ulp.  Exact-integer cases must match bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_precision_pretraining_amax_b300 import synth
+from tests.helpers import check_gemm_tiles, host_input, random_codes, random_scales, sample_tiles, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fb():
+    from fp8_precision_pretraining_amax_b300 import fp8bq
+    return fp8bq
+
+
+def _all_tiles(rows, cols):
+    return [(i, j) for i in range(rows // 128) for j in range(cols // 128)]
+
+
+def _fprop(fb, xq, sx, wq, sw):
+    y = fb.gemm_fprop(to_dev(xq), to_dev(sx), to_dev(wq), to_dev(sw))
+    fb.check()
+    return y
+
+
+def _dgrad(fb, dyq, sdy, wq, sw):
+    wqT = np.ascontiguousarray(wq.T)
+    dx = fb.gemm_dgrad(to_dev(dyq), to_dev(sdy), to_dev(wqT), to_dev(sw))
+    fb.check()
+    return dx
+
+
+def _wgrad(fb, dyqT, sdyT, xqT, sxT):
+    dw = fb.gemm_wgrad(to_dev(dyqT), to_dev(sdyT), to_dev(xqT), to_dev(sxT))
+    fb.check()
+    return dw
+
+
+def test_tiny_config_fprop_all_tiles(fb):
+    lin = synth.tiny()
+    xq, sx = oracle.quantize_rowwise(lin.x.numpy())
+    wq, _, sw = oracle.quantize_weight_block(lin.w.numpy())
+    y = _fprop(fb, xq, sx, wq, sw)
+    assert y.shape == (256, 384)
+    check_gemm_tiles(y, oracle.gemm_fprop, (xq, sx, wq, sw), _all_tiles(256, 384), what="tiny fprop")
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (128, 256, 256), (256, 384, 1152), (640, 640, 384),
+                                   (2048, 2560, 512)])
+def test_fprop_random_codes(fb, M, N, K):
+    rng = np.random.default_rng(M + N + K)
+    xq, wq = random_codes(rng, (M, K)), random_codes(rng, (N, K))
+    sx, sw = random_scales(rng, (K // 128, M)), random_scales(rng, (N // 128, K // 128))
+    y = _fprop(fb, xq, sx, wq, sw)
+    picks = _all_tiles(M, N) if M * N <= 640 * 640 else sample_tiles(rng, M, N, 12)
+    check_gemm_tiles(y, oracle.gemm_fprop, (xq, sx, wq, sw), picks, what=f"fprop {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (256, 384, 640), (384, 1024, 256)])
+def test_dgrad_random_codes(fb, M, N, K):
+    rng = np.random.default_rng(7 * M + N + K)
+    dyq, wq = random_codes(rng, (M, N)), random_codes(rng, (N, K))
+    sdy, sw = random_scales(rng, (N // 128, M)), random_scales(rng, (N // 128, K // 128))
+    dx = _dgrad(fb, dyq, sdy, wq, sw)
+    assert dx.shape == (M, K)
+    check_gemm_tiles(dx, oracle.gemm_dgrad, (dyq, sdy, wq, sw), _all_tiles(M, K), what=f"dgrad {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (640, 384, 256), (256, 256, 640)])
+def test_wgrad_random_codes(fb, M, N, K):
+    rng = np.random.default_rng(11 * M + N + K)
+    dyqT, xqT = random_codes(rng, (N, M)), random_codes(rng, (K, M))
+    sdyT, sxT = random_scales(rng, (M // 128, N)), random_scales(rng, (M // 128, K))
+    dw = _wgrad(fb, dyqT, sdyT, xqT, sxT)
+    assert dw.shape == (N, K)
+    check_gemm_tiles(dw, oracle.gemm_wgrad, (dyqT, sdyT, xqT, sxT), _all_tiles(N, K), what=f"wgrad {M}x{N}x{K}")
+
+
+def _integer_operands(rng, shape):
+    ints = np.array([-3, -2, -1, 0, 1, 2, 3], dtype=np.float32)
+    vals = rng.choice(ints, size=shape, p=[0.05, 0.1, 0.15, 0.4, 0.15, 0.1, 0.05]).astype(np.float32)
+    return oracle.e4m3_encode(vals), vals.astype(np.int64)
+
+
+def test_exact_integer_cases_are_bit_exact(fb):
+    """s = 1 (or a power of two) and small integers: every partial sum is exact
+    in FP32, so the BF16 output must equal the oracle's RNE rounding bit for bit.
+    Pins layout, indexing and scale wiring independently of the tolerance."""
+    rng = np.random.default_rng(21)
+    M, N, K = 384, 640, 512
+    xq, xv = _integer_operands(rng, (M, K))
+    wq, wv = _integer_operands(rng, (N, K))
+    sx = np.exp2(rng.integers(-2, 3, size=(K // 128, M))).astype(np.float32)
+    sw = np.exp2(rng.integers(-2, 3, size=(N // 128, K // 128))).astype(np.float32)
+    y = _fprop(fb, xq, sx, wq, sw)
+    exact, _ = oracle.gemm_fprop(xq, sx, wq, sw)
+    assert np.array_equal(synth.bf16_bits(y), oracle.bf16_from_double(exact))
+
+    dyq, _ = _integer_operands(rng, (M, N))
+    sdy = np.exp2(rng.integers(-2, 3, size=(N // 128, M))).astype(np.float32)
+    wq2, _ = _integer_operands(rng, (N, K))
+    dx = _dgrad(fb, dyq, sdy, wq2, sw)
+    exact, _ = oracle.gemm_dgrad(dyq, sdy, wq2, sw)
+    assert np.array_equal(synth.bf16_bits(dx), oracle.bf16_from_double(exact))
+
+    Mt = 512
+    dyqT, _ = _integer_operands(rng, (N, Mt))
+    xqT, _ = _integer_operands(rng, (K, Mt))
+    sdyT = np.exp2(rng.integers(-2, 3, size=(Mt // 128, N))).astype(np.float32)
+    sxT = np.exp2(rng.integers(-2, 3, size=(Mt // 128, K))).astype(np.float32)
+    dw = _wgrad(fb, dyqT, sdyT, xqT, sxT)
+    exact, _ = oracle.gemm_wgrad(dyqT, sdyT, xqT, sxT)
+    assert np.array_equal(synth.bf16_bits(dw), oracle.bf16_from_double(exact))
+
+
+def test_single_nonzero_chunk_and_scale_selection(fb):
+    rng = np.random.default_rng(22)
+    M, N, K = 256, 512, 640
+    xq, _ = _integer_operands(rng, (M, K))
+    wq, _ = _integer_operands(rng, (N, K))
+    xq[:, :384] = 0
+    xq[:, 512:] = 0                                      # only chunk 3 is nonzero
+    sx = np.ones((K // 128, M), np.float32)
+    sx[3] = np.exp2(np.arange(M) % 7 - 3).astype(np.float32)
+    sx[1] = 1024.0                                        # scales of zero chunks must not leak
+    sw = np.exp2(rng.integers(-3, 4, size=(N // 128, K // 128))).astype(np.float32)
+    y = _fprop(fb, xq, sx, wq, sw)
+    exact, _ = oracle.gemm_fprop(xq, sx, wq, sw)
+    assert np.array_equal(synth.bf16_bits(y), oracle.bf16_from_double(exact))
+
+
+def test_empty_reduction_writes_zeros(fb):
+    dev = "cuda"
+    y = torch.full((128, 256), 7.0, dtype=torch.bfloat16, device=dev)
+    e8 = torch.empty((128, 0), dtype=torch.uint8, device=dev)
+    fb.fp8bq_gemm_fprop(e8, torch.empty((0, 128), dtype=torch.float32, device=dev),
+                        torch.empty((256, 0), dtype=torch.uint8, device=dev),
+                        torch.empty((2, 0), dtype=torch.float32, device=dev), y)
+    fb.check()
+    assert torch.count_nonzero(y).item() == 0
+
+
+def test_config_qkv_1p7b_fprop_from_real_distribution(fb):
+    """Qwen3-1.7B QKV Fprop (M=8192, K=2048, N=4096): activations with outlier
+    channels quantized by the oracle, sampled 128x128 output tiles."""
+    lin = synth.qkv_1p7b()
+    xq, sx = oracle.quantize_rowwise(host_input(lin.x))
+    wq, _, sw = oracle.quantize_weight_block(host_input(lin.w))
+    y = _fprop(fb, xq, sx, wq, sw)
+    rng = np.random.default_rng(23)
+    worst = check_gemm_tiles(y, oracle.gemm_fprop, (xq, sx, wq, sw), sample_tiles(rng, 8192, 4096, 12),
+                             what="qkv fprop")
+    assert worst <= 1.0
+
+
+@pytest.mark.slow
+def test_full_size_up_proj_backward_sampled(fb):
+    """Backward of the 2048 -> 6144 up-projection at 16384 tokens: Dgrad
+    (reduce 6144) and Wgrad (reduce 16384) on random codes/scales of the full
+    shapes, checked on sampled tiles."""
+    rng = np.random.default_rng(24)
+    M, N, K = 16384, 6144, 2048
+    dyq, wq = random_codes(rng, (M, N)), random_codes(rng, (N, K))
+    sdy, sw = random_scales(rng, (N // 128, M)), random_scales(rng, (N // 128, K // 128))
+    dx = _dgrad(fb, dyq, sdy, wq, sw)
+    check_gemm_tiles(dx, oracle.gemm_dgrad, (dyq, sdy, wq, sw), sample_tiles(rng, M, K, 6), what="dgrad full")
+    dyqT = np.ascontiguousarray(dyq.T)
+    xqT = random_codes(rng, (K, M))
+    sdyT, sxT = random_scales(rng, (M // 128, N)), random_scales(rng, (M // 128, K))
+    dw = _wgrad(fb, dyqT, sdyT, xqT, sxT)
+    check_gemm_tiles(dw, oracle.gemm_wgrad, (dyqT, sdyT, xqT, sxT), sample_tiles(rng, N, K, 4), what="wgrad full")

@@ -1,0 +1,194 @@
+"""GPU parity of the three quantizers with the oracle: codes and scales must
+match bit for bit (the quantization rule has exactly one correct answer)."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_precision_pretraining_amax_b300 import synth
+from tests.conftest import GOLDEN
+from tests.helpers import assert_codes_equal, assert_scales_equal, host_input
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fb():
+    from fp8_precision_pretraining_amax_b300 import fp8bq
+    return fp8bq
+
+
+def _rowwise_parity(fb, x: torch.Tensor, what: str):
+    q, s = fb.quantize_rowwise(x)
+    fb.check()
+    qo, so = oracle.quantize_rowwise(host_input(x))
+    assert_codes_equal(q.cpu().numpy(), qo, what + " codes")
+    assert_scales_equal(s.cpu().numpy(), so, what + " scales")
+
+
+def _special_bf16(rows: int, cols: int, seed: int) -> torch.Tensor:
+    """Tiles that hit the edges of the rule: zero and -0 tiles, subnormal-only
+    tiles (FP32 scale itself subnormal), huge values, exact E4M3 midpoints."""
+    gen = synth.generator(seed)
+    x = synth.gaussian((rows, cols), 1.0, gen)
+    t = oracle.e4m3_table()[:0x7F]
+    mids = torch.from_numpy(((t[:-1] + t[1:]) / 2).astype(np.float32))
+    for r in range(rows):
+        kind = r % 9
+        seg = slice(0, 128)
+        if kind == 0:
+            x[r, seg] = 0.0
+        elif kind == 1:
+            x[r, seg] = -0.0
+        elif kind == 2:
+            x[r, seg] *= 2.0 ** -130           # BF16 subnormals: s is an FP32 subnormal
+        elif kind == 3:
+            x[r, seg] *= 1e37                  # near the top of the BF16 range
+        elif kind == 4:
+            x[r, :126] = mids * torch.where(torch.arange(126) % 2 == 0, 1.0, -1.0)
+            x[r, 126] = 448.0                  # s = 1: every midpoint is a tie
+            x[r, 127] = -0.0
+        elif kind == 5:
+            x[r, seg] = 2.0 ** -133            # a constant tile at the smallest BF16 subnormal
+        elif kind == 6:
+            x[r, seg] *= 2.0 ** -120
+    return x.to(torch.bfloat16)
+
+
+def test_rowwise_worked_tile(fb):
+    x = np.zeros(128, dtype=np.float32)
+    for line in open(os.path.join(GOLDEN, "rowwise_tile_worked.txt")):
+        p = line.split()
+        if p and p[0].isdigit():
+            x[int(p[0])] = float(p[1])
+    for dt in (torch.float32, torch.bfloat16):
+        _rowwise_parity(fb, torch.from_numpy(x).reshape(1, 128).to(dt).cuda(), f"worked tile {dt}")
+
+
+def test_rowwise_tiny_fp32(fb):
+    _rowwise_parity(fb, synth.tiny().x.cuda(), "tiny A fp32")
+
+
+@pytest.mark.parametrize("R,C", [(1, 128), (3, 256), (333, 1152), (1024, 2048)])
+def test_rowwise_bf16_activations(fb, R, C):
+    gen = synth.generator(100 + R)
+    _rowwise_parity(fb, synth.activations(R, C, gen).cuda(), f"rowwise {R}x{C}")
+
+
+def test_rowwise_special_values(fb):
+    _rowwise_parity(fb, _special_bf16(72, 384, 5).cuda(), "rowwise specials")
+    xf = _special_bf16(36, 256, 6).float()
+    xf[0, :128] *= 2.0 ** -20                  # FP32-only magnitudes
+    _rowwise_parity(fb, xf.cuda(), "rowwise specials fp32")
+
+
+def test_rowwise_pitched_input(fb):
+    gen = synth.generator(7)
+    big = synth.activations(96, 768, gen).cuda()
+    x = big[:, 128:640]                        # ldx = 768 > C = 512
+    q, s = fb.quantize_rowwise(x)
+    qo, so = oracle.quantize_rowwise(host_input(x.contiguous()))
+    assert_codes_equal(q.cpu().numpy(), qo, "pitched codes")
+    assert_scales_equal(s.cpu().numpy(), so, "pitched scales")
+
+
+def test_rowwise_empty_and_ragged(fb):
+    x = torch.zeros((0, 256), dtype=torch.bfloat16, device="cuda")
+    q, s = fb.quantize_rowwise(x)
+    assert q.shape == (0, 256) and s.shape == (2, 0)
+    bad = torch.zeros((4, 200), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(fb.Fp8bqError) as e:
+        fb.fp8bq_quantize_rowwise(bad, torch.empty((4, 200), dtype=torch.uint8, device="cuda"),
+                                  torch.empty((1, 4), dtype=torch.float32, device="cuda"))
+    assert e.value.status == fb.ERR_SHAPE
+
+
+def _colwise_parity(fb, x: torch.Tensor, what: str):
+    qT, s = fb.quantize_colwise(x)
+    fb.check()
+    qo, so = oracle.quantize_colwise(host_input(x))
+    assert_codes_equal(qT.cpu().numpy(), qo, what + " codes")
+    assert_scales_equal(s.cpu().numpy(), so, what + " scales")
+
+
+@pytest.mark.parametrize("M,C", [(128, 8), (384, 136), (256, 1024), (1024, 2056)])
+def test_colwise_bf16(fb, M, C):
+    gen = synth.generator(200 + C)
+    _colwise_parity(fb, synth.activations(M, C, gen).cuda(), f"colwise {M}x{C}")
+
+
+def test_colwise_grads_and_fp32(fb):
+    gen = synth.generator(8)
+    _colwise_parity(fb, synth.grads(512, 384, gen).cuda(), "colwise dY")
+    _colwise_parity(fb, synth.gaussian((256, 72), 0.3, gen).cuda(), "colwise fp32")
+
+
+def test_colwise_special_values(fb):
+    x = _special_bf16(384, 256, 9)
+    _colwise_parity(fb, x.t().contiguous().cuda(), "colwise specials")
+
+
+def test_colwise_equals_rowwise_of_transpose_on_gpu(fb):
+    gen = synth.generator(10)
+    x = synth.activations(512, 768, gen).cuda()
+    qT, s_col = fb.quantize_colwise(x)
+    q_row, s_row = fb.quantize_rowwise(x.t().contiguous())
+    assert torch.equal(qT, q_row) and torch.equal(s_col, s_row)
+
+
+def _weight_parity(fb, w: torch.Tensor, what: str, transpose=True):
+    q, qT, s = fb.quantize_weight_block(w, transpose=transpose)
+    fb.check()
+    qo, qTo, so = oracle.quantize_weight_block(host_input(w))
+    assert_codes_equal(q.cpu().numpy(), qo, what + " codes")
+    if transpose:
+        assert_codes_equal(qT.cpu().numpy(), qTo, what + " transposed codes")
+    assert_scales_equal(s.cpu().numpy(), so, what + " scales")
+
+
+def test_weight_block_tiny_fp32(fb):
+    _weight_parity(fb, synth.tiny().w.cuda(), "tiny W fp32")
+
+
+@pytest.mark.parametrize("N,K", [(128, 128), (384, 640), (4096, 2048)])
+def test_weight_block_bf16(fb, N, K):
+    gen = synth.generator(300 + N)
+    w = synth.weight(N, K, gen)
+    w[:128, :128] = 0.0
+    _weight_parity(fb, w.cuda(), f"weight {N}x{K}")
+
+
+def test_weight_block_without_transpose_and_specials(fb):
+    _weight_parity(fb, _special_bf16(256, 384, 11).cuda(), "weight specials", transpose=False)
+    _weight_parity(fb, _special_bf16(256, 384, 12).cuda(), "weight specials T")
+
+
+@pytest.mark.slow
+def test_full_size_quantizers_sampled(fb):
+    """Full-size tensors of the 3.8B layer / up-projection backward, checked on
+    sampled rows (row-wise), sampled columns (column-wise) and in full for the
+    weight; the launch configuration is the one the benchmark uses."""
+    rng = np.random.default_rng(13)
+    gen = synth.generator(14, "cuda")
+    dy = synth.grads(16384, 6144, gen, "cuda")
+    x = synth.activations(32768, 3072, gen, "cuda")
+    w = synth.weight(16384, 3072, gen, "cuda")
+    # row-wise on dY: 64 sampled rows with all their tiles
+    q, s = fb.quantize_rowwise(dy)
+    rows = np.sort(rng.choice(16384, 64, replace=False))
+    rows[0], rows[-1] = 0, 16383
+    qo, so = oracle.quantize_rowwise(host_input(dy[torch.from_numpy(rows).cuda()]))
+    assert_codes_equal(q[torch.from_numpy(rows).cuda()].cpu().numpy(), qo, "full rowwise codes")
+    assert_scales_equal(s[:, torch.from_numpy(rows).cuda()].cpu().numpy(), so, "full rowwise scales")
+    # column-wise on X: 32 sampled columns over all 32768 tokens
+    qT, sc = fb.quantize_colwise(x)
+    cols = np.sort(rng.choice(3072, 32, replace=False))
+    cols[0], cols[-1] = 0, 3071
+    xc = x[:, torch.from_numpy(cols).cuda()].contiguous()
+    qTo, sco = oracle.quantize_colwise(host_input(xc))
+    assert_codes_equal(qT[torch.from_numpy(cols).cuda()].cpu().numpy(), qTo, "full colwise codes")
+    assert_scales_equal(sc[:, torch.from_numpy(cols).cuda()].cpu().numpy(), sco, "full colwise scales")
+    # weight block in full (50M elements)
+    _weight_parity(fb, w, "full weight 16384x3072")
