@@ -1,0 +1,520 @@
+"""Benchmark of the block-scaled FP8 linear layer on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--tokens M]
+                    [--impl reference]
+
+One step is one pass of the whole hot path over one batch: for every linear
+of the workload, the weight-block quantizer (with the transposed copy), the
+row-wise quantizer of X, Fprop, the row-wise quantizer of dY, Dgrad, the
+column-wise quantizers of dY and X, and Wgrad.
+
+Metric: FP8 block-scaled GEMM TFLOP/s including quantization = sum of 2*M*N*K
+over the step's GEMMs divided by the step time (quantizers included), plus
+that number as a fraction of the FP8 tensor peak.  FLOPs count only the
+GEMMs.  Inputs are synthetic BF16 tensors resident in HBM; the step's working
+set (several GB) is far larger than the 126 MB L2, so no flush is needed.
+
+Default workload (layer_3p8b): one 3.8B-shaped transformer layer at 32768
+tokens (hidden 3072, 32 q / 8 kv heads of 96, SwiGLU FFN 8192): QKV
+3072->4608, O 3072->3072, gate+up 3072->16384, down 8192->3072.
+
+Also reported: per-launch CUDA-event times (the roofline of the GEMM kernel
+against the FP8 tensor peak, the quantizers against HBM), the same metric
+end to end through the Python API with pinned host buffers (host->device
+copies of X, W, dY and device->host copies of Y, dX, dW inside the timed
+region), and the CPU oracle timed on a bounded sample on the host cores.
+
+Multi-GPU (torchrun): every rank runs its own replica of the workload (the
+linears shard over tokens with no exchange for Fprop/Dgrad; a data-parallel
+Wgrad all-reduce belongs to the optimizer step, outside this path), so
+scaling is weak; the timed region is bracketed by barriers and the max over
+ranks is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "FP8 block-scaled GEMM TFLOP/s (incl. quantize) and % of B300 FP8 peak"
+UNIT = "TFLOP/s"
+TOKENS = {"layer_3p8b": 32768, "qkv_1p7b": 8192, "tiny": 256}
+FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 / 2.25 PFLOP/s)
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="layer_3p8b", choices=sorted(TOKENS))
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override the token count M of the workload (e.g. a smaller case for ncu)")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# workload description (shapes only; tensors come from synth)
+# ---------------------------------------------------------------------------
+
+def workload_shapes(name, tokens=None):
+    from fp8_precision_pretraining_amax_b300 import synth
+    M = tokens or TOKENS[name]
+    if name == "layer_3p8b":
+        return [(n, M, K, N) for n, K, N in synth.LAYER_3P8B]
+    if name == "qkv_1p7b":
+        return [("qkv", M, 2048, 4096)]
+    return [("tiny", M, 512, 384)]
+
+
+def workload_config(name, tokens=None):
+    shapes = workload_shapes(name, tokens)
+    desc = {
+        "layer_3p8b": "3.8B-shaped layer: QKV 3072->4608, O 3072->3072, gate+up 3072->16384, down 8192->3072; "
+                      "Fprop+Dgrad+Wgrad each with all quantizers",
+        "qkv_1p7b": "Qwen3-1.7B QKV layer 2048->4096; Fprop+Dgrad+Wgrad with all quantizers",
+        "tiny": "tiny 512 -> 384 layer; Fprop+Dgrad+Wgrad with all quantizers",
+    }[name]
+    return {"workload": name, "description": desc, "tokens": shapes[0][1],
+            "linears": {n: {"M": M, "K": K, "N": N} for n, M, K, N in shapes}}
+
+
+def step_flops(shapes):
+    return sum(3 * 2 * M * N * K for _, M, K, N in shapes)
+
+
+def make_inputs(name, device, tokens=None):
+    """BF16 X, W, dY per linear, generated on `device`."""
+    from fp8_precision_pretraining_amax_b300 import synth
+    M = tokens or TOKENS[name]
+    if name == "layer_3p8b":
+        return synth.layer_3p8b(device, M=M)
+    if name == "qkv_1p7b":
+        lin = synth.qkv_1p7b(device, M=M)
+        lin.dy = synth.grads(lin.M, lin.N, synth.generator(11, device), device)
+        return [lin]
+    gen = synth.generator(0, device)
+    return [synth.Linear("tiny", M, 512, 384, x=synth.activations(M, 512, gen, device),
+                         w=synth.weight(384, 512, gen, device), dy=synth.grads(M, 384, gen, device))]
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def nvsmi_id(local_rank):
+    """nvidia-smi --id of the CUDA device this rank uses (its UUID when known)."""
+    try:
+        import torch
+        u = str(torch.cuda.get_device_properties(local_rank).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        if vis:
+            return vis.split(",")[local_rank].strip()
+        return str(local_rank)
+
+
+class ClockSampler:
+    def __init__(self, local_rank):
+        self.gpu = nvsmi_id(local_rank)
+        self.proc = None
+        self.path = os.path.join("/tmp", f"fp8bq_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={CLOCK_QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows), "samples": len(rows), "reasons": reasons}
+
+
+# ---------------------------------------------------------------------------
+# peaks and the committed ncu traffic record
+# ---------------------------------------------------------------------------
+
+def peaks():
+    try:
+        mp = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        return {"hbm_gbs": mp["hbm_gbs"], "bf16_burst": mp["bf16_tflops"],
+                "bf16_sustained": mp.get("bf16_tflops_sustained", mp["bf16_tflops"]), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6400.0, "bf16_burst": 1800.0, "bf16_sustained": 1400.0, "source": "fallback"}
+
+
+def gemm_traffic_record():
+    """DRAM bytes per GEMM launch from the committed ncu summary; valid only
+    while the kernel source is unchanged (its sha256 is recorded there)."""
+    src = os.path.join(ROOT, "fp8_precision_pretraining_amax_b300", "csrc", "gemm.cuh")
+    rec = os.path.join(ROOT, "profiles", "gemm_block_scaled_layer_3p8b_traffic.txt")
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        kv = {}
+        for line in open(rec):
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                kv[k.strip()] = v.strip()
+        return kv if kv.get("gemm_cuh_sha256") == sha else None
+    except OSError:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def step_launches(fp8bq, L, lin):
+    """(kind, algorithmic work, call) for one linear's 8 launches, in step order.
+    Work: FLOPs for GEMMs, bytes read + written for quantizers."""
+    M, K, N = L.M, L.K, L.N
+    return [
+        ("quant_weight", 2 * N * K + 2 * N * K + 4 * (N // 128) * (K // 128),
+         lambda: fp8bq.fp8bq_quantize_weight_block(lin.w, L.wq, L.wqT, L.sw)),
+        ("quant_rowwise", 3 * M * K + 4 * M * (K // 128), lambda: fp8bq.fp8bq_quantize_rowwise(lin.x, L.xq, L.sx)),
+        ("gemm_fprop", 2 * M * N * K, lambda: fp8bq.fp8bq_gemm_fprop(L.xq, L.sx, L.wq, L.sw, L.y)),
+        ("quant_rowwise", 3 * M * N + 4 * M * (N // 128),
+         lambda: fp8bq.fp8bq_quantize_rowwise(lin.dy, L.dyq, L.sdy)),
+        ("gemm_dgrad", 2 * M * N * K, lambda: fp8bq.fp8bq_gemm_dgrad(L.dyq, L.sdy, L.wqT, L.sw, L.dx)),
+        ("quant_colwise", 3 * M * N + 4 * (M // 128) * N,
+         lambda: fp8bq.fp8bq_quantize_colwise(lin.dy, L.dyqT, L.sdyT)),
+        ("quant_colwise", 3 * M * K + 4 * (M // 128) * K,
+         lambda: fp8bq.fp8bq_quantize_colwise(lin.x, L.xqT, L.sxT)),
+        ("gemm_wgrad", 2 * M * N * K, lambda: fp8bq.fp8bq_gemm_wgrad(L.dyqT, L.sdyT, L.xqT, L.sxT, L.dw)),
+    ]
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from fp8_precision_pretraining_amax_b300 import fp8bq
+    from fp8_precision_pretraining_amax_b300.linear import LinearFP8
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    shapes = workload_shapes(args.workload, args.tokens)
+    lins = make_inputs(args.workload, dev, args.tokens)
+    layers = [LinearFP8(l.M, l.K, l.N, device=dev) for l in lins]
+    plan = [step_launches(fp8bq, L, lin) for L, lin in zip(layers, lins)]
+    torch.cuda.synchronize()
+    flops = step_flops(shapes)
+    launches_per_step = sum(len(p) for p in plan)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    def step(record=None):
+        for launches in plan:
+            for kind, work, fn in launches:
+                if record is None:
+                    fn()
+                else:
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    fn()
+                    e1.record()
+                    record.append((kind, work, e0, e1))
+
+    for _ in range(args.warmup):
+        step()
+    fp8bq.check(dev)
+    torch.cuda.synchronize()
+
+    # timed region: K steps on the launching (current) stream
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(args.steps):
+            step()
+        t1.record()
+        torch.cuda.synchronize()
+    barrier()
+    dev_ms = t0.elapsed_time(t1)
+    fp8bq.check(dev)
+
+    # per-launch CUDA events on the same stream (kernel durations for the roofline)
+    rec = []
+    torch.cuda.synchronize()
+    for _ in range(args.steps):
+        step(rec)
+    torch.cuda.synchronize()
+    per_kind = {}
+    for kind, work, e0, e1 in rec:
+        d = per_kind.setdefault(kind, {"launches": 0, "ms": 0.0, "work": 0})
+        d["launches"] += 1
+        d["ms"] += e0.elapsed_time(e1)
+        d["work"] += work
+
+    if world > 1:
+        t = torch.tensor([dev_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        dev_ms = float(t.item())
+    ms_per_step = dev_ms / args.steps
+    value = flops * world * args.steps / (dev_ms * 1e-3) / 1e12
+
+    e2e = None if args.no_e2e else run_e2e(args, lins, layers, dev, flops, world, barrier)
+
+    if rank != 0:
+        return None
+    pk = peaks()
+    fp8_sus = pk["bf16_sustained"] * FP8_OVER_BF16
+    fp8_burst = pk["bf16_burst"] * FP8_OVER_BF16
+    gk = [v for k, v in per_kind.items() if k.startswith("gemm")]
+    qk = [v for k, v in per_kind.items() if k.startswith("quant")]
+    g_ms, g_fl, g_n = sum(v["ms"] for v in gk), sum(v["work"] for v in gk), sum(v["launches"] for v in gk)
+    q_ms, q_by = sum(v["ms"] for v in qk), sum(v["work"] for v in qk)
+    achieved = g_fl / (g_ms * 1e-3) / 1e12
+    tr = gemm_traffic_record()
+    traffic = None
+    if tr is not None and tr.get("workload") == args.workload and args.tokens in (None, TOKENS[args.workload]):
+        traffic = float(tr["dram_bytes_per_launch"])
+    breakdown = {}
+    for k, v in sorted(per_kind.items()):
+        b = {"launches_per_step": v["launches"] // args.steps, "ms_per_step": v["ms"] / args.steps}
+        if k.startswith("gemm"):
+            b["tflops"] = v["work"] / (v["ms"] * 1e-3) / 1e12
+        else:
+            b["gbs"] = v["work"] / (v["ms"] * 1e-3) / 1e9
+            b["frac_of_hbm"] = b["gbs"] / pk["hbm_gbs"]
+        breakdown[k] = b
+    breakdown["gemm_only_tflops"] = achieved
+    breakdown["quantizers"] = {"gbs": q_by / (q_ms * 1e-3) / 1e9,
+                               "frac_of_hbm": q_by / (q_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                               "ms_per_step": q_ms / args.steps}
+    cfg = workload_config(args.workload, args.tokens)
+    cfg["parallelism"] = f"replicas x{world}" if world > 1 else "single GPU"
+    cfg["l2"] = "inputs larger than L2 (no flush)" if args.workload != "tiny" else "inputs fit in L2"
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32 accumulate -> bf16", "data": "synthetic",
+        "config": cfg,
+        "pct_of_fp8_peak": 100.0 * value / fp8_sus,
+        "roofline": {"bound": "tensor", "kernel": "gemm_block_scaled_kernel (Fprop/Dgrad/Wgrad)",
+                     "achieved": achieved, "peak": fp8_sus, "unit": "TFLOP/s", "frac": achieved / fp8_sus,
+                     "traffic": traffic,
+                     "peak_note": (f"FP8 = 2 x {pk['source']} sustained cuBLAS bf16 ({pk['bf16_sustained']} "
+                                   f"TFLOP/s); the burst-based FP8 peak would be {fp8_burst:.0f}"),
+                     "launches_per_step": g_n // args.steps},
+        "breakdown": breakdown,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if e2e is not None:
+        out["e2e"] = e2e
+    if not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(lins)
+    return out
+
+
+def run_e2e(args, lins, layers, dev, flops, world, barrier):
+    """Same step through the Python API from pinned host buffers and back."""
+    import torch
+    from fp8_precision_pretraining_amax_b300 import fp8bq
+
+    host_in = [(l.x.cpu().pin_memory(), l.w.cpu().pin_memory(), l.dy.cpu().pin_memory()) for l in lins]
+    host_out = [(torch.empty(L.y.shape, dtype=torch.bfloat16).pin_memory(),
+                 torch.empty(L.dx.shape, dtype=torch.bfloat16).pin_memory(),
+                 torch.empty(L.dw.shape, dtype=torch.bfloat16).pin_memory()) for L in layers]
+    dev_in = [(torch.empty_like(l.x), torch.empty_like(l.w), torch.empty_like(l.dy)) for l in lins]
+    h2d = sum(t.numel() * t.element_size() for trio in host_in for t in trio)
+    d2h = sum(t.numel() * t.element_size() for trio in host_out for t in trio)
+
+    def e2e_step():
+        for (hx, hw, hdy), (dx_, dw_, ddy), L, (oy, odx, odw) in zip(host_in, dev_in, layers, host_out):
+            dx_.copy_(hx, non_blocking=True)
+            dw_.copy_(hw, non_blocking=True)
+            ddy.copy_(hdy, non_blocking=True)
+            L.step(dx_, dw_, ddy)
+            oy.copy_(L.y, non_blocking=True)
+            odx.copy_(L.dx, non_blocking=True)
+            odw.copy_(L.dw, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    steps = max(1, min(args.steps, 5))
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    barrier()
+    fp8bq.check(dev)
+    if world > 1:
+        t = torch.tensor([dt], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        dt = float(t.item())
+    return {"value": flops * world * steps / dt / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": 1e3 * dt / steps,
+            "path": "pinned host -> device copies, LinearFP8.step (C-ABI), device -> pinned host copies"}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle: the baseline leg and the reference arm
+# ---------------------------------------------------------------------------
+
+def host_slices(lins, tile):
+    """The operand slices the oracle sample needs, copied to the host."""
+    from fp8_precision_pretraining_amax_b300 import synth
+    out = []
+    for l in lins:
+        out.append(((l.name, l.M, l.K, l.N), (
+            synth.bf16_bits(l.x[:tile]),                    # tile rows of X, all K
+            synth.bf16_bits(l.x[:, :128].contiguous()),     # 128 columns of X, all tokens
+            synth.bf16_bits(l.w[:128]),                     # one N block of W, all K
+            synth.bf16_bits(l.w[:, :128].contiguous()),     # one K block of W, all N
+            synth.bf16_bits(l.dy[:tile]),                   # tile rows of dY
+            synth.bf16_bits(l.dy[:, :128].contiguous()))))  # 128 columns of dY, all tokens
+    return out
+
+
+def oracle_sample(slices, tile):
+    """Time the oracle on a bounded sample of one step and extrapolate.
+
+    For each linear: quantize the operand slices that one tile x tile output
+    block of Fprop, Dgrad and Wgrad needs, then compute those three blocks.
+    Quantizer seconds per element and GEMM seconds per multiply-add are
+    scaled to the full step's element and multiply-add counts."""
+    import numpy as np
+    import oracle
+
+    q_time = g_time = 0.0
+    q_elems = g_macs = full_q = full_macs = 0
+    for (_, M, K, N), (xr, xc, wr, wc, dyr, dyc) in slices:
+        full_q += 2 * M * K + 2 * M * N + N * K  # row-wise X, dY; column-wise dY, X; weight
+        full_macs += 3 * M * N * K
+        t = time.perf_counter()
+        xq, sx = oracle.quantize_rowwise(xr)
+        wq, _, sw = oracle.quantize_weight_block(wr)
+        dyq, sdy = oracle.quantize_rowwise(dyr)
+        wq2, _, sw2 = oracle.quantize_weight_block(wc)
+        dyqT, sdyT = oracle.quantize_colwise(dyc)
+        xqT, sxT = oracle.quantize_colwise(xc)
+        q_time += time.perf_counter() - t
+        q_elems += xr.size + wr.size + dyr.size + wc.size + dyc.size + xc.size
+        idx = np.arange(tile)
+        t = time.perf_counter()
+        oracle.gemm_fprop(xq, sx, wq, sw, rows=idx, cols=idx)
+        oracle.gemm_dgrad(dyq, sdy, wq2, sw2, rows=idx, cols=idx)
+        oracle.gemm_wgrad(dyqT, sdyT, xqT, sxT, rows=idx, cols=idx)
+        g_time += time.perf_counter() - t
+        g_macs += tile * tile * (K + N + M)
+    est = full_q * (q_time / q_elems) + full_macs * (g_time / g_macs)
+    return {"tflops": 2 * full_macs / est / 1e12, "sample_seconds": q_time + g_time, "step_seconds": est}
+
+
+def cpu_baseline(lins, tile=64):
+    import oracle
+    r = oracle_sample(host_slices(lins, tile), tile)
+    return {"value": r["tflops"], "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": (f"per linear one {tile}x{tile} output block of Fprop, Dgrad and Wgrad plus the "
+                       f"quantization of the operand slices it needs ({r['sample_seconds']:.1f} s of CPU "
+                       f"work), extrapolated to the full step ({r['step_seconds']:.0f} s)")}
+
+
+def run_reference(args):
+    """The oracle as it stands on the host cores, same metric and config."""
+    import oracle
+    import torch
+    device = "cuda" if torch.cuda.is_available() else "cpu"  # input generation only
+    tile = 64
+    lins = make_inputs(args.workload, device, args.tokens)
+    sl = host_slices(lins, tile)
+    del lins
+    vals = [oracle_sample(sl, tile) for _ in range(args.warmup + args.steps)][args.warmup:]
+    value = statistics.median(v["tflops"] for v in vals)
+    est = statistics.median(v["step_seconds"] for v in vals)
+    cfg = workload_config(args.workload, args.tokens)
+    cfg["parallelism"] = "host cores (oracle)"
+    sample = (f"each step: per linear one {tile}x{tile} output block of Fprop, Dgrad and Wgrad plus the "
+              f"quantization of the operand slices it needs; time extrapolated to the full step")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": est * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64 oracle (E4M3 codes, FP32 scales)",
+            "data": "synthetic", "config": cfg,
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ---------------------------------------------------------------------------
+
+def main(argv=None):
+    args = parse_args(argv)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return 0
+
+    import torch
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    out = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

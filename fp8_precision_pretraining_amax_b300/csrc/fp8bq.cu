@@ -96,6 +96,19 @@ int encode_u8_map(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t ou
     return r == CUDA_SUCCESS ? FP8BQ_OK : FP8BQ_ERR_CUDA;
 }
 
+// 2-D BF16 output [rows][cols] (dense), store boxes of 32 rows x 64 columns
+// (128-byte rows) with 128-byte swizzle, matching the epilogue staging.
+int encode_bf16_out_map(CUtensorMap* map, void* ptr, uint64_t cols, uint64_t rows) {
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {64, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides, box, estr,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FP8BQ_OK : FP8BQ_ERR_CUDA;
+}
+
 template <int MODE>
 int run_gemm(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, uint16_t* D, int64_t I,
              int64_t J, int64_t Kr, cudaStream_t stream) {
@@ -116,9 +129,10 @@ int run_gemm(const uint8_t* A, const float* sA, const uint8_t* B, const float* s
                                                                                             : FP8BQ_ERR_CUDA;
     }
 
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, td;
     if (encode_u8_map(&ta, A, Kr, I, fp8bq::kBM) != FP8BQ_OK) return FP8BQ_ERR_CUDA;
     if (encode_u8_map(&tb, B, Kr, J, fp8bq::kBN) != FP8BQ_OK) return FP8BQ_ERR_CUDA;
+    if (encode_bf16_out_map(&td, D, J, I) != FP8BQ_OK) return FP8BQ_ERR_CUDA;
 
     fp8bq::GemmParams p;
     p.sA = sA;
@@ -134,7 +148,7 @@ int run_gemm(const uint8_t* A, const float* sA, const uint8_t* B, const float* s
     p.timeout_ns = kDefaultTimeoutNs;
     const int grid = static_cast<int>(tiles < dev->sms ? tiles : dev->sms);
     fp8bq::gemm_block_scaled_kernel<MODE>
-        <<<grid, fp8bq::kGemmThreads, fp8bq::kGemmSmemBytes, stream>>>(ta, tb, p, dev->status);
+        <<<grid, fp8bq::kGemmThreads, fp8bq::kGemmSmemBytes, stream>>>(ta, tb, td, p, dev->status);
     return launch_status();
 }
 

@@ -45,13 +45,17 @@ enum GemmMode : int { kModeFprop = 0, kModeDgrad = 1, kModeWgrad = 2 };
 constexpr int kBM = 128;          // tile rows (TMEM lanes)
 constexpr int kBN = 256;          // tile columns (MMA N)
 constexpr int kBK = 128;          // one scale chunk of the reduction
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr int kGemmThreads = 384;
 constexpr int kFirstPromoWarp = 4;
 constexpr int kPromoWarps = 8;
 constexpr uint32_t kStageBytesA = kBM * kBK;
 constexpr uint32_t kStageBytesB = kBN * kBK;
 constexpr uint32_t kTmemCols = 2 * kBN;
+// Epilogue staging: per promotion warp 32 rows x 128 BF16 columns as two
+// 32 x 64 boxes of 128-byte rows, 128-byte swizzled for the TMA store.
+constexpr uint32_t kEpiBoxBytes = 32 * 128;
+constexpr uint32_t kEpiWarpBytes = 2 * kEpiBoxBytes;
 
 struct GemmParams {
     const float* sA;
@@ -74,7 +78,8 @@ struct alignas(16) GemmCtl {
     float sbw[kPromoWarps][2][128];  // Wgrad column scales: [warp][chunk parity][column]
 };
 
-constexpr size_t kGemmSmemBytes = 1024 + kStages * (kStageBytesA + kStageBytesB) + sizeof(GemmCtl);
+constexpr size_t kGemmSmemBytes =
+    1024 + kStages * (kStageBytesA + kStageBytesB) + kPromoWarps * kEpiWarpBytes + sizeof(GemmCtl);
 
 // One lane waits, the verdict is broadcast so the warp stays converged.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
@@ -105,12 +110,14 @@ __device__ __forceinline__ float chunk_scale_b(const GemmParams& p, int c, int j
 template <int MODE>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_block_scaled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                             const GemmParams p, unsigned int* __restrict__ status) {
+                             const __grid_constant__ CUtensorMap tmD, const GemmParams p,
+                             unsigned int* __restrict__ status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* smA = base;
     uint8_t* smB = base + kStages * kStageBytesA;
-    GemmCtl* ctl = reinterpret_cast<GemmCtl*>(smB + kStages * kStageBytesB);
+    uint8_t* smEpi = smB + kStages * kStageBytesB;
+    GemmCtl* ctl = reinterpret_cast<GemmCtl*>(smEpi + kPromoWarps * kEpiWarpBytes);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -129,6 +136,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         fence_barrier_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmD);
     }
     if (warp == 1) {
         tmem_alloc(smem_addr(&ctl->tmem_base), kTmemCols);
@@ -230,6 +238,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 tc_fence_after();
                 const uint32_t tbase = tmem + lane_off + buf * kBN + half * 128;
                 if (MODE != kModeWgrad) {
+                    // acc += (sA * sB) * partial, two columns per packed FMA
                     const float sab = sa * sb;
 #pragma unroll
                     for (int g = 0; g < 2; ++g) {
@@ -239,14 +248,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         tmem_wait_ld();
                         reg_fence32(r0);
                         reg_fence32(r1);
+                        float* a = acc + g * 64;
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            acc[g * 64 + i] = fmaf(sab, __uint_as_float(r0[i]), acc[g * 64 + i]);
-                            acc[g * 64 + 32 + i] = fmaf(sab, __uint_as_float(r1[i]), acc[g * 64 + 32 + i]);
+                        for (int i = 0; i < 32; i += 2) {
+                            ffma2(a[i], a[i + 1], sab, sab, __uint_as_float(r0[i]), __uint_as_float(r0[i + 1]));
+                            ffma2(a[32 + i], a[33 + i], sab, sab, __uint_as_float(r1[i]), __uint_as_float(r1[i + 1]));
                         }
                     }
                 } else {
-                    // per-column scales: acc += (sa * sB[j]) * partial
+                    // per-column scales: acc += sA * (sB[j] * partial)
 #pragma unroll
                     for (int g = 0; g < 4; ++g) {
                         uint32_t r0[32];
@@ -254,13 +264,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         tmem_wait_ld();
                         reg_fence32(r0);
                         const float* sbv = &ctl->sbw[pw][it & 1][g * 32];
+                        float* a = acc + g * 32;
 #pragma unroll
                         for (int i = 0; i < 32; i += 4) {
                             const float4 b = *reinterpret_cast<const float4*>(sbv + i);
-                            acc[g * 32 + i + 0] = fmaf(sa * b.x, __uint_as_float(r0[i + 0]), acc[g * 32 + i + 0]);
-                            acc[g * 32 + i + 1] = fmaf(sa * b.y, __uint_as_float(r0[i + 1]), acc[g * 32 + i + 1]);
-                            acc[g * 32 + i + 2] = fmaf(sa * b.z, __uint_as_float(r0[i + 2]), acc[g * 32 + i + 2]);
-                            acc[g * 32 + i + 3] = fmaf(sa * b.w, __uint_as_float(r0[i + 3]), acc[g * 32 + i + 3]);
+                            float t0, t1, t2, t3;
+                            fmul2(t0, t1, __uint_as_float(r0[i]), __uint_as_float(r0[i + 1]), b.x, b.y);
+                            fmul2(t2, t3, __uint_as_float(r0[i + 2]), __uint_as_float(r0[i + 3]), b.z, b.w);
+                            ffma2(a[i], a[i + 1], t0, t1, sa, sa);
+                            ffma2(a[i + 2], a[i + 3], t2, t3, sa, sa);
                         }
                     }
                 }
@@ -271,19 +283,35 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 if (buf == 0) tph ^= 1;
             }
             if (!ok) break;
-            if (hv) {
-                uint4* drow = reinterpret_cast<uint4*>(p.D + static_cast<int64_t>(gi) * p.J + jh);
+            // Epilogue: round to BF16 into this warp's swizzled staging boxes,
+            // then one lane issues the TMA stores (asynchronous: they drain
+            // while the next tile's chunks are promoted).
+            uint8_t* stg = smEpi + pw * kEpiWarpBytes;
+            if (lane == 0) bulk_wait_group_read<0>();  // the previous tile's stores left the buffer
+            __syncwarp();
 #pragma unroll
-                for (int v = 0; v < 16; ++v) {
+            for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float* a = acc + h * 64 + j * 8;
                     uint4 o;
-                    o.x = pack_bf16x2(acc[8 * v + 0], acc[8 * v + 1]);
-                    o.y = pack_bf16x2(acc[8 * v + 2], acc[8 * v + 3]);
-                    o.z = pack_bf16x2(acc[8 * v + 4], acc[8 * v + 5]);
-                    o.w = pack_bf16x2(acc[8 * v + 6], acc[8 * v + 7]);
-                    drow[v] = o;
+                    o.x = pack_bf16x2(a[0], a[1]);
+                    o.y = pack_bf16x2(a[2], a[3]);
+                    o.z = pack_bf16x2(a[4], a[5]);
+                    o.w = pack_bf16x2(a[6], a[7]);
+                    *reinterpret_cast<uint4*>(stg + h * kEpiBoxBytes + lane * 128 + ((j ^ (lane & 7)) << 4)) = o;
                 }
             }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0 && hv) {
+                const int y0 = tm * kBM + quarter * 32;
+                tma_store_2d(&tmD, smem_addr(stg), jh, y0);
+                tma_store_2d(&tmD, smem_addr(stg + kEpiBoxBytes), jh + 64, y0);
+                bulk_commit_group();
+            }
         }
+        if (lane == 0) bulk_wait_group<0>();  // all output writes complete before exit
         if (!ok) raise_abort(ctl, status);
     }
 
