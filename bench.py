@@ -4,9 +4,10 @@
                     [--impl reference]
 
 One step is one pass of the whole hot path over one batch: for every linear
-of the workload, the weight-block quantizer (with the transposed copy), the
-row-wise quantizer of X, Fprop, the row-wise quantizer of dY, Dgrad, the
-column-wise quantizers of dY and X, and Wgrad.
+of the workload, the weight-block quantizer (with the transposed copy), one
+pass over X producing its row-wise (Fprop) and column-wise (Wgrad) codes,
+Fprop, one pass over dY producing its row-wise (Dgrad) and column-wise
+(Wgrad) codes, Dgrad and Wgrad.
 
 Metric: FP8 block-scaled GEMM TFLOP/s including quantization = sum of 2*M*N*K
 over the step's GEMMs divided by the step time (quantizers included), plus
@@ -211,21 +212,19 @@ def gemm_traffic_record():
 # ---------------------------------------------------------------------------
 
 def step_launches(fp8bq, L, lin):
-    """(kind, algorithmic work, call) for one linear's 8 launches, in step order.
-    Work: FLOPs for GEMMs, bytes read + written for quantizers."""
+    """(kind, algorithmic work, call) for one linear's 6 launches, in step order.
+    Work: FLOPs for GEMMs, bytes read + written for quantizers (BF16 in, one
+    code byte per layout, one FP32 scale per 128 elements and layout)."""
     M, K, N = L.M, L.K, L.N
+    rowcol = lambda R, C: 2 * R * C + 2 * R * C + 4 * R * (C // 128) + 4 * (R // 128) * C
     return [
         ("quant_weight", 2 * N * K + 2 * N * K + 4 * (N // 128) * (K // 128),
          lambda: fp8bq.fp8bq_quantize_weight_block(lin.w, L.wq, L.wqT, L.sw)),
-        ("quant_rowwise", 3 * M * K + 4 * M * (K // 128), lambda: fp8bq.fp8bq_quantize_rowwise(lin.x, L.xq, L.sx)),
+        ("quant_rowcol", rowcol(M, K), lambda: fp8bq.fp8bq_quantize_rowcol(lin.x, L.xq, L.sx, L.xqT, L.sxT)),
         ("gemm_fprop", 2 * M * N * K, lambda: fp8bq.fp8bq_gemm_fprop(L.xq, L.sx, L.wq, L.sw, L.y)),
-        ("quant_rowwise", 3 * M * N + 4 * M * (N // 128),
-         lambda: fp8bq.fp8bq_quantize_rowwise(lin.dy, L.dyq, L.sdy)),
+        ("quant_rowcol", rowcol(M, N),
+         lambda: fp8bq.fp8bq_quantize_rowcol(lin.dy, L.dyq, L.sdy, L.dyqT, L.sdyT)),
         ("gemm_dgrad", 2 * M * N * K, lambda: fp8bq.fp8bq_gemm_dgrad(L.dyq, L.sdy, L.wqT, L.sw, L.dx)),
-        ("quant_colwise", 3 * M * N + 4 * (M // 128) * N,
-         lambda: fp8bq.fp8bq_quantize_colwise(lin.dy, L.dyqT, L.sdyT)),
-        ("quant_colwise", 3 * M * K + 4 * (M // 128) * K,
-         lambda: fp8bq.fp8bq_quantize_colwise(lin.x, L.xqT, L.sxT)),
         ("gemm_wgrad", 2 * M * N * K, lambda: fp8bq.fp8bq_gemm_wgrad(L.dyqT, L.sdyT, L.xqT, L.sxT, L.dw)),
     ]
 

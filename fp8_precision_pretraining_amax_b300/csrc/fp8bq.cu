@@ -34,6 +34,21 @@ std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
+// The FP32 slab (64 KB) exceeds the default 48 KB of dynamic shared memory.
+template <bool kF32>
+cudaError_t set_tile_smem() {
+    const int bytes = fp8bq::tile_smem_bytes<kF32>();
+    cudaError_t e = cudaFuncSetAttribute(fp8bq::quantize_tile_kernel<kF32, fp8bq::kTileCol>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(fp8bq::quantize_tile_kernel<kF32, fp8bq::kTileDual>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(fp8bq::quantize_tile_kernel<kF32, fp8bq::kTileWeight>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    return e;
+}
+
 int probe_device(DeviceState** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return FP8BQ_ERR_CUDA;
@@ -60,6 +75,7 @@ int probe_device(DeviceState** out) {
                 cudaFuncSetAttribute(fp8bq::gemm_block_scaled_kernel<fp8bq::kModeWgrad>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
                 return FP8BQ_ERR_CUDA;
+            if (set_tile_smem<false>() != cudaSuccess || set_tile_smem<true>() != cudaSuccess) return FP8BQ_ERR_CUDA;
             if (g_encode == nullptr) {
                 void* fn = nullptr;
                 cudaDriverEntryPointQueryResult q;
@@ -107,6 +123,20 @@ int encode_bf16_out_map(CUtensorMap* map, void* ptr, uint64_t cols, uint64_t row
                                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? FP8BQ_OK : FP8BQ_ERR_CUDA;
+}
+
+// One 128x128 slab per CTA: grid (ceil(C/128), R/128).
+template <int kMode>
+int launch_tile(const void* x, int dtype, int64_t R, int64_t C, int64_t ldx, uint8_t* q, float* s_row, uint8_t* qT,
+                float* s_col, cudaStream_t cs) {
+    dim3 grid(static_cast<unsigned>((C + 127) / 128), static_cast<unsigned>(R / 128));
+    if (dtype == FP8BQ_BF16)
+        fp8bq::quantize_tile_kernel<false, kMode>
+            <<<grid, 256, fp8bq::tile_smem_bytes<false>(), cs>>>(x, R, C, ldx, q, s_row, qT, s_col);
+    else
+        fp8bq::quantize_tile_kernel<true, kMode>
+            <<<grid, 256, fp8bq::tile_smem_bytes<true>(), cs>>>(x, R, C, ldx, q, s_row, qT, s_col);
+    return launch_status();
 }
 
 template <int MODE>
@@ -184,18 +214,29 @@ int fp8bq_quantize_colwise(const void* x, int dtype, int64_t M, int64_t C, int64
     if (M == 0 || C == 0) return FP8BQ_OK;
     if (!x || !qT || !s) return FP8BQ_ERR_NULL;
     if (!aligned16(x) || !aligned16(qT) || !aligned16(s) || ((ldx * elem_size(dtype)) % 16)) return FP8BQ_ERR_ALIGN;
-    if (M / 128 > 65535) return FP8BQ_ERR_SHAPE;
+    if (M / 128 > 65535 || (C + 127) / 128 >= (int64_t(1) << 31)) return FP8BQ_ERR_SHAPE;
     DeviceState* dev = nullptr;
     int st = probe_device(&dev);
     if (st != FP8BQ_OK) return st;
-    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    const int cw = dtype == FP8BQ_BF16 ? 128 : 64;
-    dim3 grid(static_cast<unsigned>((C + cw - 1) / cw), static_cast<unsigned>(M / 128));
-    if (dtype == FP8BQ_BF16)
-        fp8bq::quantize_colwise_kernel<false><<<grid, 256, 0, cs>>>(x, M, C, ldx, qT, s);
-    else
-        fp8bq::quantize_colwise_kernel<true><<<grid, 256, 0, cs>>>(x, M, C, ldx, qT, s);
-    return launch_status();
+    return launch_tile<fp8bq::kTileCol>(x, dtype, M, C, ldx, nullptr, nullptr, qT, s,
+                                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fp8bq_quantize_rowcol(const void* x, int dtype, int64_t M, int64_t C, int64_t ldx, uint8_t* q, float* s_row,
+                          uint8_t* qT, float* s_col, fp8bq_stream_t stream) {
+    if (dtype != FP8BQ_BF16 && dtype != FP8BQ_F32) return FP8BQ_ERR_DTYPE;
+    if (M < 0 || C < 0 || ldx < C || (M % 128) || (C % 128)) return FP8BQ_ERR_SHAPE;
+    if (M == 0 || C == 0) return FP8BQ_OK;
+    if (!x || !q || !s_row || !qT || !s_col) return FP8BQ_ERR_NULL;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(s_row) || !aligned16(qT) || !aligned16(s_col) ||
+        ((ldx * elem_size(dtype)) % 16))
+        return FP8BQ_ERR_ALIGN;
+    if (M / 128 > 65535 || C / 128 >= (int64_t(1) << 31)) return FP8BQ_ERR_SHAPE;
+    DeviceState* dev = nullptr;
+    int st = probe_device(&dev);
+    if (st != FP8BQ_OK) return st;
+    return launch_tile<fp8bq::kTileDual>(x, dtype, M, C, ldx, q, s_row, qT, s_col,
+                                         reinterpret_cast<cudaStream_t>(stream));
 }
 
 int fp8bq_quantize_weight_block(const void* w, int dtype, int64_t N, int64_t K, int64_t ldw, uint8_t* q,
@@ -211,13 +252,8 @@ int fp8bq_quantize_weight_block(const void* w, int dtype, int64_t N, int64_t K, 
     DeviceState* dev = nullptr;
     int st = probe_device(&dev);
     if (st != FP8BQ_OK) return st;
-    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>(N / 128));
-    if (dtype == FP8BQ_BF16)
-        fp8bq::quantize_weight_block_kernel<false><<<grid, 256, 0, cs>>>(w, N, K, ldw, q, qT, s);
-    else
-        fp8bq::quantize_weight_block_kernel<true><<<grid, 256, 0, cs>>>(w, N, K, ldw, q, qT, s);
-    return launch_status();
+    return launch_tile<fp8bq::kTileWeight>(w, dtype, N, K, ldw, q, s, qT, nullptr,
+                                           reinterpret_cast<cudaStream_t>(stream));
 }
 
 int fp8bq_gemm_fprop(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw, uint16_t* y, int64_t M,

@@ -6,14 +6,22 @@
 // amax == 0); code = E4M3(x / s) where x / s is the correctly rounded FP32
 // quotient and E4M3() rounds half to even with saturation to +-448.
 //
-// Every kernel reads its input exactly once with 128-bit (or 32-bit
-// column-pair) coalesced loads, reduces amax in registers and warp shuffles,
-// and writes codes and scales once.
+// Two kernel families, both reading their input exactly once:
+//   quantize_rowwise_kernel  streams 1x128 tiles straight from HBM with
+//                            128-bit coalesced loads (no shared memory).
+//   quantize_tile_kernel     stages a 128x128 slab in shared memory with
+//                            16-byte cp.async copies and serves every layout
+//                            that needs columns: column-wise 128x1 tiles
+//                            emitted transposed, the fused row-wise +
+//                            column-wise pass over one slab, and 128x128
+//                            weight blocks (row-major and transposed codes).
 #pragma once
 
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
+
+#include "ptx.cuh"
 
 namespace fp8bq {
 
@@ -27,18 +35,58 @@ __device__ __forceinline__ float tile_scale(float amax) {
     return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
 }
 
-// Two quotients -> two E4M3 codes packed low byte first (element a first).
-__device__ __forceinline__ uint32_t e4m3x2(float a, float b, float s) {
-    float2 v = make_float2(__fdiv_rn(a, s), __fdiv_rn(b, s));
-    return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3));
+// Below this tile amax the reciprocal-based quotient is not guaranteed to be
+// the correctly rounded one (the residual x - q0 s can fall into the FP32
+// subnormal range and lose bits), so such tiles use IEEE division.  Checked
+// exhaustively over every pair of BF16 values (x, amax), |x| <= amax.
+constexpr float kRecipMinAmax = 0x1p-80f;
+
+// Per-tile divisor: the scale, its correctly rounded reciprocal, and whether
+// the one-step reciprocal quotient applies.
+struct TileDiv {
+    float s, ns, r;
+    bool fast;
+};
+
+__device__ __forceinline__ TileDiv tile_div(float amax) {
+    TileDiv d;
+    d.s = tile_scale(amax);
+    d.ns = -d.s;
+    d.r = __frcp_rn(d.s);
+    d.fast = amax >= kRecipMinAmax;
+    return d;
 }
 
-// Eight values -> eight codes in two 32-bit words (memory order).
-__device__ __forceinline__ uint2 e4m3x8(const float (&v)[8], float s) {
-    uint2 o;
-    o.x = e4m3x2(v[0], v[1], s) | (e4m3x2(v[2], v[3], s) << 16);
-    o.y = e4m3x2(v[4], v[5], s) | (e4m3x2(v[6], v[7], s) << 16);
-    return o;
+// Sign of x copied onto q: x / s carries the sign of x (s > 0), which the
+// correction step below loses for x = -0 only.
+__device__ __forceinline__ float with_sign_of(float q, float x) {
+    return __uint_as_float(__float_as_uint(q) | (__float_as_uint(x) & 0x80000000u));
+}
+
+// Two correctly rounded quotients a / s, b / s.  Fast path (Markstein's
+// division theorem, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990): with r = RN(1/s),
+// q0 = RN(x r) lies within one ulp of x / s, the residual x - q0 s is exact
+// under FMA, and q0 + r (x - q0 s) rounded once is RN(x / s).  Packed f32x2
+// arithmetic, two quotients per instruction.
+__device__ __forceinline__ float2 quot2(float a, float b, const TileDiv& d) {
+    if (!d.fast) return make_float2(__fdiv_rn(a, d.s), __fdiv_rn(b, d.s));
+    float q0a, q0b;
+    fmul2(q0a, q0b, a, b, d.r, d.r);
+    float ea = a, eb = b;
+    ffma2(ea, eb, q0a, q0b, d.ns, d.ns);  // e = x - q0 s (exact)
+    ffma2(q0a, q0b, ea, eb, d.r, d.r);    // q = q0 + e r
+    return make_float2(with_sign_of(q0a, a), with_sign_of(q0b, b));
+}
+
+// Two values -> two E4M3 codes packed low byte first (element a first).
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b, const TileDiv& d) {
+    return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(quot2(a, b, d), __NV_SATFINITE, __NV_E4M3));
+}
+
+// Four values -> four codes in one 32-bit word (memory order).
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float e, const TileDiv& d) {
+    return e4m3x2(a, b, d) | (e4m3x2(c, e, d) << 16);
 }
 
 __device__ __forceinline__ void unpack_bf16x8(const uint4& w, float (&v)[8]) {
@@ -56,10 +104,13 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
     return r;
 }
 
-__device__ __forceinline__ uint32_t ldg_nc_u32(const void* p) {
-    uint32_t r;
-    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
-    return r;
+// 16-byte global -> shared copy that bypasses L1; src_bytes = 0 zero-fills.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ row-wise
@@ -116,180 +167,207 @@ __global__ void __launch_bounds__(256) quantize_rowwise_kernel(const void* __res
     amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
     amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
-    const float sc = tile_scale(amax);
+    const TileDiv d = tile_div(amax);
 
     if (!valid) return;
     uint8_t* dst = q + r * C + t * 128;
     if (!kF32) {
-        float a[8], b[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) { a[i] = v[i]; b[i] = v[8 + i]; }
-        *reinterpret_cast<uint2*>(dst + 8 * j) = e4m3x8(a, sc);
-        *reinterpret_cast<uint2*>(dst + 64 + 8 * j) = e4m3x8(b, sc);
+        *reinterpret_cast<uint2*>(dst + 8 * j) =
+            make_uint2(e4m3x4(v[0], v[1], v[2], v[3], d), e4m3x4(v[4], v[5], v[6], v[7], d));
+        *reinterpret_cast<uint2*>(dst + 64 + 8 * j) =
+            make_uint2(e4m3x4(v[8], v[9], v[10], v[11], d), e4m3x4(v[12], v[13], v[14], v[15], d));
     } else {
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            uint32_t w = e4m3x2(v[4 * p], v[4 * p + 1], sc) | (e4m3x2(v[4 * p + 2], v[4 * p + 3], sc) << 16);
-            *reinterpret_cast<uint32_t*>(dst + 32 * p + 4 * j) = w;
-        }
+        for (int p = 0; p < 4; ++p)
+            *reinterpret_cast<uint32_t*>(dst + 32 * p + 4 * j) =
+                e4m3x4(v[4 * p], v[4 * p + 1], v[4 * p + 2], v[4 * p + 3], d);
     }
-    if (j == 0) s[t * R + r] = sc;
+    if (j == 0) s[t * R + r] = d.s;
 }
 
-// --------------------------------------------------------------- column-wise
+// ------------------------------------------------------------- 128x128 slabs
 //
-// CTA = 256 threads over a slab of 128 tokens x (64 * VEC) columns, VEC = 2
-// for BF16 (a thread owns a column pair, 4-byte loads) and 1 for FP32.
-// Thread (g = tid % 64, quarter = tid / 64) loads tokens [32*quarter, +32) of
-// its column(s): each warp-wide load covers 128 contiguous bytes of one row.
-// The per-column amax is combined across the four quarters in shared memory,
-// and each thread writes its 32 codes per column as 32 contiguous bytes of
-// the transposed output row qT[c][m].
+// CTA = 256 threads, one slab of 128 rows x 128 columns (rows r0.., columns
+// c0..; all 128 rows exist, trailing columns past C read as zero and are not
+// written).  The slab is copied to shared memory with 16-byte cp.async
+// (row pitch 128 * element size), then read in two ways, both free of bank
+// conflicts because every warp access covers contiguous bytes of one row:
+//   column view  thread = (4-byte unit u of a row, group g of rows): BF16 has
+//                64 units (column pairs) x 4 groups of 32 rows, FP32 128
+//                units (columns) x 2 groups of 64 rows.  Per-column amax over
+//                the group, combined over groups in shared memory; codes of
+//                a column's rows are contiguous in the transposed output.
+//   row view     8 lanes per row, 16 values per lane (the row-wise kernel's
+//                mapping), 32 rows per pass, 4 passes.
+// Modes:
+//   kTileCol     column-wise 128x1 tiles: qT [C][R], s_col [R/128][C]
+//   kTileDual    row-wise 1x128 and column-wise 128x1 tiles of the same
+//                slab: q [R][C], s_row [C/128][R], qT, s_col (one read of x)
+//   kTileWeight  one 128x128 block: q [R][C], qT [C][R] (optional),
+//                s_row = block scales [R/128][C/128]
+
+enum TileMode : int { kTileCol = 0, kTileDual = 1, kTileWeight = 2 };
 
 template <bool kF32>
-__global__ void __launch_bounds__(256) quantize_colwise_kernel(const void* __restrict__ x, int64_t M, int64_t C,
-                                                               int64_t ldx, uint8_t* __restrict__ qT,
-                                                               float* __restrict__ s) {
-    constexpr int VEC = kF32 ? 1 : 2;
-    constexpr int CW = 64 * VEC;  // columns per CTA
-    __shared__ float red[4][CW];
+constexpr int tile_smem_bytes() { return 128 * 128 * (kF32 ? 4 : 2); }
+
+template <bool kF32, int kMode>
+__global__ void __launch_bounds__(256) quantize_tile_kernel(const void* __restrict__ x, int64_t R, int64_t C,
+                                                            int64_t ldx, uint8_t* __restrict__ q,
+                                                            float* __restrict__ s_row, uint8_t* __restrict__ qT,
+                                                            float* __restrict__ s_col) {
+    constexpr int E = kF32 ? 4 : 2;
+    constexpr int RB = 128 * E;       // slab row pitch in shared memory (bytes)
+    constexpr int CPR = RB / 16;      // 16-byte chunks per row
+    constexpr int UPR = RB / 4;       // 4-byte units per row (column view)
+    constexpr int VEC = 4 / E;        // columns per unit
+    constexpr int G = 256 / UPR;      // row groups (column view)
+    constexpr int RPG = 128 / G;      // rows per group
+    extern __shared__ __align__(16) uint8_t slab[];
+    __shared__ float red[G][128];
+    __shared__ float wred[8];
 
     const int tid = threadIdx.x;
-    const int g = tid & 63;
-    const int quarter = tid >> 6;
-    const int64_t m0 = static_cast<int64_t>(blockIdx.y) * 128;
-    const int64_t c = static_cast<int64_t>(blockIdx.x) * CW + g * VEC;  // first column of this thread
-    const bool valid = c < C;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 128;
+    const uint8_t* xb = static_cast<const uint8_t*>(x);
 
-    float v[VEC][32];
-    if (!kF32) {
-        const uint16_t* src = static_cast<const uint16_t*>(x) + (m0 + quarter * 32) * ldx + c;
+    // ---- stage the slab
+    const uint32_t sbase = smem_addr(slab);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            uint32_t w = valid ? ldg_nc_u32(src + i * ldx) : 0u;
-            v[0][i] = bf16lo(w);
-            v[1 % VEC][i] = bf16hi(w);
-        }
-    } else {
-        const float* src = static_cast<const float*>(x) + (m0 + quarter * 32) * ldx + c;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[0][i] = valid ? __uint_as_float(ldg_nc_u32(src + i * ldx)) : 0.0f;
+    for (int k = 0; k < (128 * CPR) / 256; ++k) {
+        const int i = tid + 256 * k;
+        const int row = i / CPR, ch = i % CPR;
+        const int64_t col = c0 + ch * (16 / E);
+        const bool ok = col < C;
+        const uint8_t* src = xb + ((r0 + row) * ldx + (ok ? col : c0)) * E;
+        cp_async_16(sbase + row * RB + ch * 16, src, ok ? 16u : 0u);
     }
-
-    float amax[VEC];
-#pragma unroll
-    for (int e = 0; e < VEC; ++e) {
-        float a = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) a = fmaxf(a, fabsf(v[e][i]));
-        red[quarter][g * VEC + e] = a;
-    }
+    cp_async_wait_all();
     __syncthreads();
-    float sc[VEC];
-#pragma unroll
-    for (int e = 0; e < VEC; ++e) {
-        const int col = g * VEC + e;
-        amax[e] = fmaxf(fmaxf(red[0][col], red[1][col]), fmaxf(red[2][col], red[3][col]));
-        sc[e] = tile_scale(amax[e]);
-    }
-    if (!valid) return;
 
+    // ---- column view: amax of this thread's column(s) over its row group
+    const int u = tid % UPR, g = tid / UPR;
+    const uint8_t* colp = slab + g * RPG * RB + u * 4;
+    float cmax[VEC];
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) {
-        uint32_t w[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            w[i] = e4m3x2(v[e][4 * i], v[e][4 * i + 1], sc[e]) | (e4m3x2(v[e][4 * i + 2], v[e][4 * i + 3], sc[e]) << 16);
-        uint8_t* dst = qT + (c + e) * M + m0 + quarter * 32;
-        reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        if (quarter == 0) s[blockIdx.y * C + c + e] = sc[e];
-    }
-}
-
-// ------------------------------------------------------------- weight block
-//
-// One CTA (256 threads) per 128x128 block.  Thread t owns the 8x8 sub-block
-// rows [8a, 8a+8), columns [8b, 8b+8) with a = t / 16, b = t % 16: a warp's
-// loads of one sub-block row cover two full 256-byte block rows.  The block
-// amax goes through warp shuffles and shared memory.  Codes are written
-// row-major (q) and, from the same quotients paired down the columns,
-// transposed (qT), so q and qT hold bit-identical codes.
-
-template <bool kF32>
-__global__ void __launch_bounds__(256) quantize_weight_block_kernel(const void* __restrict__ w, int64_t N,
-                                                                    int64_t K, int64_t ldw, uint8_t* __restrict__ q,
-                                                                    uint8_t* __restrict__ qT,
-                                                                    float* __restrict__ s) {
-    __shared__ float red[8];
-    const int tid = threadIdx.x;
-    const int a = tid >> 4, b = tid & 15;
-    const int64_t n0 = static_cast<int64_t>(blockIdx.y) * 128 + 8 * a;  // first row of the sub-block
-    const int64_t k0 = static_cast<int64_t>(blockIdx.x) * 128 + 8 * b;  // first column
-
-    float v[8][8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int e = 0; e < VEC; ++e) cmax[e] = 0.0f;
+#pragma unroll 8
+    for (int i = 0; i < RPG; ++i) {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(colp + i * RB);
         if (!kF32) {
-            const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(w) + (n0 + i) * ldw + k0;
-            unpack_bf16x8(ldg_nc_v4(src), v[i]);
+            cmax[0] = fmaxf(cmax[0], fabsf(bf16lo(w)));
+            cmax[VEC - 1] = fmaxf(cmax[VEC - 1], fabsf(bf16hi(w)));
         } else {
-            const float* src = static_cast<const float*>(w) + (n0 + i) * ldw + k0;
-            uint4 lo = ldg_nc_v4(src), hi = ldg_nc_v4(src + 4);
-            v[i][0] = __uint_as_float(lo.x); v[i][1] = __uint_as_float(lo.y);
-            v[i][2] = __uint_as_float(lo.z); v[i][3] = __uint_as_float(lo.w);
-            v[i][4] = __uint_as_float(hi.x); v[i][5] = __uint_as_float(hi.y);
-            v[i][6] = __uint_as_float(hi.z); v[i][7] = __uint_as_float(hi.w);
+            cmax[0] = fmaxf(cmax[0], fabsf(__uint_as_float(w)));
         }
     }
-    float amax = 0.0f;
+    TileDiv cd[VEC];
+    if (kMode != kTileWeight) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+        for (int e = 0; e < VEC; ++e) red[g][u * VEC + e] = cmax[e];
+        __syncthreads();
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) amax = fmaxf(amax, fabsf(v[i][jj]));
+        for (int e = 0; e < VEC; ++e) {
+            float a = red[0][u * VEC + e];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
-    if ((tid & 31) == 0) red[tid >> 5] = amax;
-    __syncthreads();
-    amax = red[0];
-#pragma unroll
-    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
-    const float sc = tile_scale(amax);
-
-    // quotients once, then two pairings
-    float y[8][8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) y[i][jj] = __fdiv_rn(v[i][jj], sc);
-
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        uint32_t lo = 0, hi = 0;
-#pragma unroll
-        for (int p = 0; p < 2; ++p) {
-            lo |= static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(y[i][2 * p], y[i][2 * p + 1]),
-                                                                 __NV_SATFINITE, __NV_E4M3)) << (16 * p);
-            hi |= static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(y[i][4 + 2 * p], y[i][5 + 2 * p]),
-                                                                 __NV_SATFINITE, __NV_E4M3)) << (16 * p);
+            for (int gg = 1; gg < G; ++gg) a = fmaxf(a, red[gg][u * VEC + e]);
+            cd[e] = tile_div(a);
         }
-        *reinterpret_cast<uint2*>(q + (n0 + i) * K + k0) = make_uint2(lo, hi);
+    } else {
+        float a = cmax[0];
+#pragma unroll
+        for (int e = 1; e < VEC; ++e) a = fmaxf(a, cmax[e]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, off));
+        if ((tid & 31) == 0) wred[tid >> 5] = a;
+        __syncthreads();
+        a = wred[0];
+#pragma unroll
+        for (int w = 1; w < 8; ++w) a = fmaxf(a, wred[w]);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) cd[e] = tile_div(a);
+        if (tid == 0) s_row[(r0 >> 7) * (C >> 7) + (c0 >> 7)] = cd[0].s;
     }
-    if (qT != nullptr) {
+
+    // ---- column view: codes, transposed (qT[c][r0 + g*RPG ...], 16 rows per store)
+    if (kMode != kTileWeight || qT != nullptr) {
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-            uint32_t lo = 0, hi = 0;
+        for (int e = 0; e < VEC; ++e) {
+            const int64_t c = c0 + u * VEC + e;
+            if (c < C) {
+                uint8_t* dst = qT + c * R + r0 + g * RPG;
 #pragma unroll
-            for (int p = 0; p < 2; ++p) {
-                lo |= static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(y[2 * p][jj], y[2 * p + 1][jj]),
-                                                                     __NV_SATFINITE, __NV_E4M3)) << (16 * p);
-                hi |= static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(y[4 + 2 * p][jj], y[5 + 2 * p][jj]),
-                                                                     __NV_SATFINITE, __NV_E4M3)) << (16 * p);
+                for (int h = 0; h < RPG / 16; ++h) {
+                    uint32_t wv[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        float f[4];
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            const uint32_t w =
+                                *reinterpret_cast<const uint32_t*>(colp + (h * 16 + k * 4 + m) * RB);
+                            f[m] = kF32 ? __uint_as_float(w) : (e == 0 ? bf16lo(w) : bf16hi(w));
+                        }
+                        wv[k] = e4m3x4(f[0], f[1], f[2], f[3], cd[e]);
+                    }
+                    *reinterpret_cast<uint4*>(dst + h * 16) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                }
+                if (kMode != kTileWeight && g == 0) s_col[(r0 >> 7) * C + c] = cd[e].s;
             }
-            *reinterpret_cast<uint2*>(qT + (k0 + jj) * N + n0) = make_uint2(lo, hi);
         }
     }
-    if (tid == 0) s[blockIdx.y * (K >> 7) + blockIdx.x] = sc;
+
+    // ---- row view: row-wise tiles (dual) or the block's row-major codes (weight)
+    if (kMode == kTileCol) return;
+    const int j = tid & 7;
+#pragma unroll 1
+    for (int p = 0; p < 4; ++p) {
+        const int row = p * 32 + (tid >> 3);
+        const uint8_t* rp = slab + row * RB;
+        float v[16];
+        if (!kF32) {
+            float a[8], b[8];
+            unpack_bf16x8(*reinterpret_cast<const uint4*>(rp + 16 * j), a);
+            unpack_bf16x8(*reinterpret_cast<const uint4*>(rp + 16 * (j + 8)), b);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) { v[i] = a[i]; v[8 + i] = b[i]; }
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint4 w = *reinterpret_cast<const uint4*>(rp + 16 * (j + 8 * k));
+                v[4 * k + 0] = __uint_as_float(w.x);
+                v[4 * k + 1] = __uint_as_float(w.y);
+                v[4 * k + 2] = __uint_as_float(w.z);
+                v[4 * k + 3] = __uint_as_float(w.w);
+            }
+        }
+        TileDiv d;
+        if (kMode == kTileDual) {
+            float amax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
+            d = tile_div(amax);
+            if (j == 0) s_row[(c0 >> 7) * R + r0 + row] = d.s;
+        } else {
+            d = cd[0];
+        }
+        uint8_t* dst = q + (r0 + row) * C + c0;
+        if (!kF32) {
+            *reinterpret_cast<uint2*>(dst + 8 * j) =
+                make_uint2(e4m3x4(v[0], v[1], v[2], v[3], d), e4m3x4(v[4], v[5], v[6], v[7], d));
+            *reinterpret_cast<uint2*>(dst + 64 + 8 * j) =
+                make_uint2(e4m3x4(v[8], v[9], v[10], v[11], d), e4m3x4(v[12], v[13], v[14], v[15], d));
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                *reinterpret_cast<uint32_t*>(dst + 32 * k + 4 * j) =
+                    e4m3x4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3], d);
+        }
+    }
 }
 
 }  // namespace fp8bq

@@ -25,8 +25,8 @@ BF16, F32 = 0, 1
 
 #: Names of the C-ABI entry points declared in include/fp8bq.h.
 C_FUNCTIONS = (
-    "fp8bq_quantize_rowwise", "fp8bq_quantize_colwise", "fp8bq_quantize_weight_block",
-    "fp8bq_gemm_fprop", "fp8bq_gemm_dgrad", "fp8bq_gemm_wgrad",
+    "fp8bq_quantize_rowwise", "fp8bq_quantize_colwise", "fp8bq_quantize_rowcol",
+    "fp8bq_quantize_weight_block", "fp8bq_gemm_fprop", "fp8bq_gemm_dgrad", "fp8bq_gemm_wgrad",
     "fp8bq_check", "fp8bq_status_string", "fp8bq_selftest_wait_timeout",
 )
 
@@ -41,6 +41,7 @@ def _load():
     sig = {
         "fp8bq_quantize_rowwise": [vp, i32, i64, i64, i64, vp, vp, vp],
         "fp8bq_quantize_colwise": [vp, i32, i64, i64, i64, vp, vp, vp],
+        "fp8bq_quantize_rowcol": [vp, i32, i64, i64, i64, vp, vp, vp, vp, vp],
         "fp8bq_quantize_weight_block": [vp, i32, i64, i64, i64, vp, vp, vp, vp],
         "fp8bq_gemm_fprop": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
         "fp8bq_gemm_dgrad": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
@@ -137,6 +138,21 @@ def fp8bq_quantize_colwise(x: torch.Tensor, qT: torch.Tensor, s: torch.Tensor) -
                "fp8bq_quantize_colwise")
 
 
+def fp8bq_quantize_rowcol(x: torch.Tensor, q: torch.Tensor, s_row: torch.Tensor, qT: torch.Tensor,
+                          s_col: torch.Tensor) -> None:
+    """x [M, C] -> row-wise q [M, C], s_row [C/128, M] and column-wise qT [C, M], s_col [M/128, C]
+    in one pass over x (same bits as fp8bq_quantize_rowwise + fp8bq_quantize_colwise)."""
+    ldx = _rows_input(x, "x")
+    M, C = x.shape
+    _need(q, torch.uint8, (M, C), "q")
+    _need(s_row, torch.float32, (C // 128, M), "s_row")
+    _need(qT, torch.uint8, (C, M), "qT")
+    _need(s_col, torch.float32, (M // 128, C), "s_col")
+    with torch.cuda.device(x.device):
+        _raise(lib.fp8bq_quantize_rowcol(_ptr(x), _dtype_code(x), M, C, ldx, _ptr(q), _ptr(s_row), _ptr(qT),
+                                         _ptr(s_col), _stream(x)), "fp8bq_quantize_rowcol")
+
+
 def fp8bq_quantize_weight_block(w: torch.Tensor, q: torch.Tensor, qT: Optional[torch.Tensor],
                                 s: torch.Tensor) -> None:
     """w [N, K] -> q [N, K], qT [K, N] (or None), s [N/128, K/128]."""
@@ -229,6 +245,17 @@ def quantize_colwise(x: torch.Tensor) -> Tuple[torch.Tensor, torch.Tensor]:
     s = torch.empty((M // 128, C), dtype=torch.float32, device=x.device)
     fp8bq_quantize_colwise(x, qT, s)
     return qT, s
+
+
+def quantize_rowcol(x: torch.Tensor):
+    """Returns (q, s_row, qT, s_col)."""
+    M, C = x.shape
+    q = torch.empty((M, C), dtype=torch.uint8, device=x.device)
+    s_row = torch.empty((C // 128, M), dtype=torch.float32, device=x.device)
+    qT = torch.empty((C, M), dtype=torch.uint8, device=x.device)
+    s_col = torch.empty((M // 128, C), dtype=torch.float32, device=x.device)
+    fp8bq_quantize_rowcol(x, q, s_row, qT, s_col)
+    return q, s_row, qT, s_col
 
 
 def quantize_weight_block(w: torch.Tensor, transpose: bool = True):

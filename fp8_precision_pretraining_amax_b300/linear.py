@@ -5,10 +5,11 @@ main linear layers in FP8 with DeepSeek-V3-style fine-grained quantization and
 keeps everything else in BF16/FP32.  For a layer with input X [M, K], weight
 W [N, K] and output gradient dY [M, N] one training step does:
 
-  forward    X -> row-wise 1x128 codes   W -> 128x128 block codes (+ transposed)
+  forward    W -> 128x128 block codes (+ transposed)
+             X -> row-wise 1x128 codes and column-wise 128x1 codes (one pass)
              Y  = Fprop(Xq, Wq)                                         [M, N]
-  backward   dY -> row-wise 1x128 codes  dX = Dgrad(dYq, Wq^T)          [M, K]
-             dY, X -> column-wise 128x1 codes (transposed)
+  backward   dY -> row-wise and column-wise codes (one pass)
+             dX = Dgrad(dYq, Wq^T)                                      [M, K]
              dW = Wgrad(dYq^T, Xq^T)                                    [N, K]
 
 `LinearFP8` owns the code/scale buffers for one shape so that a step performs
@@ -41,25 +42,29 @@ class LinearFP8:
     def flops_per_gemm(self) -> int:
         return 2 * self.M * self.N * self.K
 
-    def forward(self, x: torch.Tensor, w: torch.Tensor) -> torch.Tensor:
+    def forward(self, x: torch.Tensor, w: torch.Tensor, for_backward: bool = True) -> torch.Tensor:
+        """Quantize W (both layouts) and X, then Fprop.  With for_backward the
+        column-wise codes of X that Wgrad needs come out of the same pass over X."""
         fp8bq.fp8bq_quantize_weight_block(w, self.wq, self.wqT, self.sw)
-        fp8bq.fp8bq_quantize_rowwise(x, self.xq, self.sx)
+        if for_backward:
+            fp8bq.fp8bq_quantize_rowcol(x, self.xq, self.sx, self.xqT, self.sxT)
+        else:
+            fp8bq.fp8bq_quantize_rowwise(x, self.xq, self.sx)
         fp8bq.fp8bq_gemm_fprop(self.xq, self.sx, self.wq, self.sw, self.y)
         return self.y
 
-    def backward(self, x: torch.Tensor, dy: torch.Tensor):
-        """Needs forward() to have quantized the weight (wqT, sw are reused)."""
-        fp8bq.fp8bq_quantize_rowwise(dy, self.dyq, self.sdy)
+    def backward(self, dy: torch.Tensor):
+        """Needs forward(for_backward=True) first (wqT, sw, xqT, sxT are reused)."""
+        fp8bq.fp8bq_quantize_rowcol(dy, self.dyq, self.sdy, self.dyqT, self.sdyT)
         fp8bq.fp8bq_gemm_dgrad(self.dyq, self.sdy, self.wqT, self.sw, self.dx)
-        fp8bq.fp8bq_quantize_colwise(dy, self.dyqT, self.sdyT)
-        fp8bq.fp8bq_quantize_colwise(x, self.xqT, self.sxT)
         fp8bq.fp8bq_gemm_wgrad(self.dyqT, self.sdyT, self.xqT, self.sxT, self.dw)
         return self.dx, self.dw
 
     def step(self, x: torch.Tensor, w: torch.Tensor, dy: torch.Tensor):
-        """Fprop + Dgrad + Wgrad: 3 GEMMs and 5 quantizer launches."""
+        """Fprop + Dgrad + Wgrad: 3 GEMMs and 3 quantizer launches (weight block,
+        row+column pass over X, row+column pass over dY)."""
         self.forward(x, w)
-        self.backward(x, dy)
+        self.backward(dy)
         return self.y, self.dx, self.dw
 
-    LAUNCHES_PER_STEP = 8
+    LAUNCHES_PER_STEP = 6

@@ -95,6 +95,21 @@ int fp8bq_quantize_colwise(const void* x, int dtype, int64_t M, int64_t C, int64
                            uint8_t* qT, float* s, fp8bq_stream_t stream);
 
 /*
+ * Row-wise 1x128 and column-wise 128x1 quantization of the same tensor in one
+ * pass over it (the output gradient dY feeds Dgrad row-wise and Wgrad
+ * column-wise; an activation X feeds Fprop row-wise and Wgrad column-wise).
+ * Writes exactly what fp8bq_quantize_rowwise(x -> q, s_row) followed by
+ * fp8bq_quantize_colwise(x -> qT, s_col) would, bit for bit, while reading x
+ * from memory once instead of twice.
+ *   x      [M][C] input of `dtype`, row pitch ldx elements (ldx >= C)
+ *   q      [M][C] row-wise codes,      s_row [C/128][M]
+ *   qT     [C][M] column-wise codes,   s_col [M/128][C]
+ * Requires M % 128 == 0 and C % 128 == 0.
+ */
+int fp8bq_quantize_rowcol(const void* x, int dtype, int64_t M, int64_t C, int64_t ldx,
+                          uint8_t* q, float* s_row, uint8_t* qT, float* s_col, fp8bq_stream_t stream);
+
+/*
  * Weight quantization per 128x128 block.
  *   w      [N][K] weight of `dtype` (nn.Linear layout), row pitch ldw elements
  *   q      [N][K] E4M3 codes (Fprop operand), dense

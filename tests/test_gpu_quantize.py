@@ -192,3 +192,106 @@ def test_full_size_quantizers_sampled(fb):
     assert_scales_equal(sc[:, torch.from_numpy(cols).cuda()].cpu().numpy(), sco, "full colwise scales")
     # weight block in full (50M elements)
     _weight_parity(fb, w, "full weight 16384x3072")
+
+
+# ---------------------------------------------------------------------------
+# fused row-wise + column-wise pass
+# ---------------------------------------------------------------------------
+
+def _rowcol_parity(fb, x: torch.Tensor, what: str):
+    q, s_row, qT, s_col = fb.quantize_rowcol(x)
+    fb.check()
+    xh = host_input(x)
+    qo, so = oracle.quantize_rowwise(xh)
+    qTo, sco = oracle.quantize_colwise(xh)
+    assert_codes_equal(q.cpu().numpy(), qo, what + " row-wise codes")
+    assert_scales_equal(s_row.cpu().numpy(), so, what + " row-wise scales")
+    assert_codes_equal(qT.cpu().numpy(), qTo, what + " column-wise codes")
+    assert_scales_equal(s_col.cpu().numpy(), sco, what + " column-wise scales")
+
+
+@pytest.mark.parametrize("M,C", [(128, 128), (384, 640), (1024, 2048)])
+def test_rowcol_bf16(fb, M, C):
+    gen = synth.generator(400 + M + C)
+    _rowcol_parity(fb, synth.activations(M, C, gen).cuda(), f"rowcol {M}x{C}")
+
+
+def test_rowcol_grads_fp32_and_specials(fb):
+    gen = synth.generator(15)
+    _rowcol_parity(fb, synth.grads(512, 768, gen).cuda(), "rowcol dY")
+    _rowcol_parity(fb, synth.gaussian((256, 384), 0.3, gen).cuda(), "rowcol fp32")
+    _rowcol_parity(fb, _special_bf16(384, 256, 16).cuda(), "rowcol specials")
+    _rowcol_parity(fb, _special_bf16(128, 384, 17).float().cuda(), "rowcol specials fp32")
+
+
+def test_rowcol_matches_separate_kernels_and_pitch(fb):
+    gen = synth.generator(18)
+    big = synth.activations(640, 1152, gen).cuda()
+    x = big[:, 128:1024]                               # ldx = 1152 > C = 896
+    q, s_row, qT, s_col = fb.quantize_rowcol(x)
+    q2, s2 = fb.quantize_rowwise(x)
+    qT2, sc2 = fb.quantize_colwise(x)
+    assert torch.equal(q, q2) and torch.equal(s_row, s2)
+    assert torch.equal(qT, qT2) and torch.equal(s_col, sc2)
+
+
+def test_rowcol_rejects_partial_tiles(fb):
+    x = torch.zeros((128, 200), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(fb.Fp8bqError) as e:
+        fb.fp8bq_quantize_rowcol(x, torch.empty((128, 200), dtype=torch.uint8, device="cuda"),
+                                 torch.empty((1, 128), dtype=torch.float32, device="cuda"),
+                                 torch.empty((200, 128), dtype=torch.uint8, device="cuda"),
+                                 torch.empty((1, 200), dtype=torch.float32, device="cuda"))
+    assert e.value.status == fb.ERR_SHAPE
+
+
+# ---------------------------------------------------------------------------
+# the quotient x / s near its hardest cases
+# ---------------------------------------------------------------------------
+
+def _every_bf16_amax(seed: int) -> torch.Tensor:
+    """One 1x128 tile per positive finite BF16 value a (32640 rows, padded):
+    element 0 is a, the rest are random BF16 values of magnitude <= a with
+    random signs, so every scale a BF16 tile can have is exercised."""
+    rng = np.random.default_rng(seed)
+    a = np.arange(1, 0x7F80, dtype=np.uint32)                # positive finite BF16 bit patterns
+    a = np.concatenate([a, a[-1:]])                           # 32640 rows = 255 x 128
+    frac = rng.random((a.size, 127))
+    mags = np.floor(frac * (a[:, None] + 1)).astype(np.uint32)  # bit patterns in [0, a]
+    signs = rng.integers(0, 2, size=mags.shape, dtype=np.uint32) << 15
+    bits = np.concatenate([a[:, None], mags | signs], axis=1).astype(np.uint16)
+    return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+
+
+def test_every_bf16_tile_scale(fb):
+    """Codes and scales for tiles of every possible BF16 amax, through the
+    row-wise, fused and column-wise kernels."""
+    x = _every_bf16_amax(19).cuda()
+    _rowwise_parity(fb, x, "every amax rowwise")
+    _rowcol_parity(fb, x[:, :128].contiguous(), "every amax rowcol")
+    _colwise_parity(fb, x.t().contiguous(), "every amax colwise")
+
+
+def test_fp32_quotients_next_to_rounding_midpoints(fb):
+    """FP32 inputs x = RN(m s) and its FP32 neighbours for every midpoint m
+    between adjacent E4M3 values and many scales s: x / s then lies within an
+    ulp or two of a rounding boundary, where only the correctly rounded
+    quotient gives the right code."""
+    rng = np.random.default_rng(20)
+    t = oracle.e4m3_table()[:0x7F].astype(np.float64)
+    mids = ((t[:-1] + t[1:]) / 2)                              # 126 midpoints, all < 448
+    rows = []
+    for _ in range(64):
+        amax = np.float32(rng.uniform(1, 2) * 2.0 ** rng.integers(-60, 60))
+        s = np.float32(amax / np.float32(448.0))
+        body = (mids * np.float64(s)).astype(np.float32)
+        for nudge in (-1, 0, 1):
+            v = body.view(np.uint32).astype(np.int64) + nudge
+            row = np.concatenate([[amax], v.astype(np.uint32).view(np.float32)[:126], [-0.0]]).astype(np.float32)
+            row[1:127] *= np.where(rng.random(126) < 0.5, -1, 1).astype(np.float32)
+            rows.append(row)
+    x = torch.from_numpy(np.stack(rows))                       # 192 x 128 FP32
+    _rowwise_parity(fb, x.cuda(), "midpoints rowwise")
+    _rowcol_parity(fb, x[:128].contiguous().cuda(), "midpoints rowcol")
+    _colwise_parity(fb, x.t().contiguous().cuda(), "midpoints colwise")
+    _weight_parity(fb, x[:128].contiguous().cuda(), "midpoints weight")
