@@ -27,8 +27,23 @@ struct DeviceState {
     bool probed = false;
     bool supported = false;
     int sms = 0;
+    int max_pairs = 0;               // co-resident GEMM clusters (CTA pairs)
     unsigned int* status = nullptr;  // device address of g_status_word
 };
+
+// Launch configuration of the GEMM: `pairs` clusters of two CTAs.
+void gemm_launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int pairs, cudaStream_t stream) {
+    cfg->gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+    cfg->blockDim = dim3(fp8bq::kGemmThreads, 1, 1);
+    cfg->dynamicSmemBytes = fp8bq::kGemmSmemBytes;
+    cfg->stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg->attrs = attr;
+    cfg->numAttrs = 1;
+}
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
@@ -76,6 +91,17 @@ int probe_device(DeviceState** out) {
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
                 return FP8BQ_ERR_CUDA;
             if (set_tile_smem<false>() != cudaSuccess || set_tile_smem<true>() != cudaSuccess) return FP8BQ_ERR_CUDA;
+            {
+                cudaLaunchConfig_t cfg = {};
+                cudaLaunchAttribute attr[1];
+                gemm_launch_config(&cfg, attr, sms / 2, nullptr);
+                int clusters = 0;
+                if (cudaOccupancyMaxActiveClusters(&clusters, fp8bq::gemm_block_scaled_kernel<fp8bq::kModeFprop>,
+                                                   &cfg) != cudaSuccess ||
+                    clusters < 1)
+                    return FP8BQ_ERR_CUDA;
+                d.max_pairs = clusters;
+            }
             if (g_encode == nullptr) {
                 void* fn = nullptr;
                 cudaDriverEntryPointQueryResult q;
@@ -112,15 +138,15 @@ int encode_u8_map(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t ou
     return r == CUDA_SUCCESS ? FP8BQ_OK : FP8BQ_ERR_CUDA;
 }
 
-// 2-D BF16 output [rows][cols] (dense), store boxes of 32 rows x 64 columns
-// (128-byte rows) with 128-byte swizzle, matching the epilogue staging.
+// 2-D BF16 output [rows][cols] (dense), store boxes of 32 rows x 32 columns
+// (64-byte rows) with 64-byte swizzle, matching the epilogue staging.
 int encode_bf16_out_map(CUtensorMap* map, void* ptr, uint64_t cols, uint64_t rows) {
     const cuuint64_t dims[2] = {cols, rows};
     const cuuint64_t strides[1] = {cols * 2};
-    const cuuint32_t box[2] = {64, 32};
+    const cuuint32_t box[2] = {32, 32};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides, box, estr,
-                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? FP8BQ_OK : FP8BQ_ERR_CUDA;
 }
@@ -161,24 +187,27 @@ int run_gemm(const uint8_t* A, const float* sA, const uint8_t* B, const float* s
 
     CUtensorMap ta, tb, td;
     if (encode_u8_map(&ta, A, Kr, I, fp8bq::kBM) != FP8BQ_OK) return FP8BQ_ERR_CUDA;
-    if (encode_u8_map(&tb, B, Kr, J, fp8bq::kBN) != FP8BQ_OK) return FP8BQ_ERR_CUDA;
+    if (encode_u8_map(&tb, B, Kr, J, fp8bq::kBNHalf) != FP8BQ_OK) return FP8BQ_ERR_CUDA;
     if (encode_bf16_out_map(&td, D, J, I) != FP8BQ_OK) return FP8BQ_ERR_CUDA;
 
     fp8bq::GemmParams p;
     p.sA = sA;
     p.sB = sB;
-    p.D = D;
     p.I = static_cast<int>(I);
     p.J = static_cast<int>(J);
     p.KC = static_cast<int>(Kr / 128);
     p.tiles_n = static_cast<int>((J + fp8bq::kBN - 1) / fp8bq::kBN);
-    const int64_t tiles = (I / fp8bq::kBM) * p.tiles_n;
+    const int64_t tiles = ((I + fp8bq::kPairM - 1) / fp8bq::kPairM) * p.tiles_n;
     if (tiles >= (int64_t(1) << 31)) return FP8BQ_ERR_SHAPE;
     p.num_tiles = static_cast<int>(tiles);
     p.timeout_ns = kDefaultTimeoutNs;
-    const int grid = static_cast<int>(tiles < dev->sms ? tiles : dev->sms);
-    fp8bq::gemm_block_scaled_kernel<MODE>
-        <<<grid, fp8bq::kGemmThreads, fp8bq::kGemmSmemBytes, stream>>>(ta, tb, td, p, dev->status);
+    // persistent: one CTA pair per TPC that can hold one, never more pairs than tiles
+    const int pairs = static_cast<int>(tiles < dev->max_pairs ? tiles : dev->max_pairs);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    gemm_launch_config(&cfg, attr, pairs, stream);
+    if (cudaLaunchKernelEx(&cfg, fp8bq::gemm_block_scaled_kernel<MODE>, ta, tb, td, p, dev->status) != cudaSuccess)
+        return FP8BQ_ERR_CUDA;
     return launch_status();
 }
 

@@ -11,27 +11,44 @@
 // which is the per-128-chunk scale promotion with FP32 accumulation that the
 // Puro-2B report's FP8 recipe (section 2, after DeepSeek-V3) relies on.
 //
-// Design (one persistent CTA per SM, 384 threads = 3 warpgroups):
-//   warp 0      TMA producer: 128x128 A tile + 256x128 B tile per chunk into a
-//               4-stage shared-memory ring (128-byte swizzle), mbarrier tx.
-//   warp 1      MMA issuer (one thread): four tcgen05.mma kind::f8f6f4
-//               (128x256x32) per chunk into one of two TMEM partial buffers
-//               of 256 FP32 columns, started fresh every chunk, then
-//               tcgen05.commit to release the smem stage and publish the
-//               partial.
+// Design: persistent clusters of two CTAs (the two SMs of a TPC), 384
+// threads each, one 256 x 256 output tile per cluster at a time, K chunk of
+// 128 (one scale chunk).  CTA rank r of the pair owns output rows
+// [128 r, 128 r + 128) of the tile and all 256 columns.
+//   warp 0      producer (both CTAs): TMA loads of this CTA's 128 rows of A
+//               and its half (128 rows) of B per chunk into a 5-stage
+//               shared-memory ring (128-byte swizzle), completion bytes
+//               counted on the even CTA's full barrier, which expects both
+//               CTAs' bytes; and cp.async copies of the chunk's scales (this
+//               CTA's 128 row scales and the tile's column scales) into an
+//               8-slot scale ring, so no promotion warp ever waits on a
+//               global-memory load.
+//   warp 1      allocates the pair's TMEM (both CTAs); in the even CTA one
+//               thread issues four tcgen05.mma.cta_group::2.kind::f8f6f4
+//               (256x256x32) per chunk into one of two TMEM partial buffers
+//               of 256 FP32 columns, started fresh every chunk, then commits
+//               with a multicast to both CTAs' stage-empty and partial-full
+//               barriers.
 //   warps 2, 3  idle (the first warpgroup gives up registers: 40 per thread)
-//   warps 4..11 promotion (two warpgroups at 232 registers per thread): each
-//               thread owns one output row and 128 columns;
-//               it reads the chunk partial from TMEM (tcgen05.ld), multiplies
-//               by the chunk's scale product and adds it into FP32 registers.
-//               While it does so the tensor core is already computing the
-//               next chunk into the other TMEM buffer.  After the last chunk
-//               the accumulators are rounded to BF16 and stored.
+//   warps 4..11 promotion (two warpgroups at 232 registers per thread, both
+//               CTAs): each thread owns one output row and 128 columns; it
+//               reads the chunk partial from its CTA's TMEM (tcgen05.ld),
+//               hands the buffer back to the MMA (the even CTA's
+//               partial-empty barrier, 16 arrivals: 8 warps per CTA) as soon
+//               as the partial is in registers, and multiplies it by the
+//               chunk's scale product into FP32 accumulators.  While it does
+//               so the tensor cores already compute the next chunk into the
+//               other buffer.  After the last chunk the accumulators are
+//               rounded to BF16 and stored with TMA.
+// Per SM and chunk this moves 32 KB through TMA and shared memory (a single
+// CTA with a 128 x 256 tile needs 48 KB) for the same tensor-core work.
 // Every wait is bounded: a stalled pipeline records FP8BQ_ERR_TIMEOUT in the
-// device status word and the CTA unwinds (draining its own in-flight copies
-// and MMAs, then freeing TMEM) instead of hanging.
+// device status word, raises the abort flag of both CTAs and the pair
+// unwinds (draining in-flight copies and MMAs, then freeing TMEM) instead of
+// hanging.
 #pragma once
 
+#include <cstddef>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -42,41 +59,58 @@ namespace fp8bq {
 
 enum GemmMode : int { kModeFprop = 0, kModeDgrad = 1, kModeWgrad = 2 };
 
-constexpr int kBM = 128;          // tile rows (TMEM lanes)
+constexpr int kBM = 128;          // tile rows per CTA (TMEM lanes)
+constexpr int kPairM = 256;       // tile rows per CTA pair
 constexpr int kBN = 256;          // tile columns (MMA N)
+constexpr int kBNHalf = 128;      // B rows each CTA loads
 constexpr int kBK = 128;          // one scale chunk of the reduction
-constexpr int kStages = 3;
+constexpr int kStages = 5;
+constexpr int kScaleSlots = 8;
 constexpr int kGemmThreads = 384;
 constexpr int kFirstPromoWarp = 4;
 constexpr int kPromoWarps = 8;
 constexpr uint32_t kStageBytesA = kBM * kBK;
-constexpr uint32_t kStageBytesB = kBN * kBK;
+constexpr uint32_t kStageBytesB = kBNHalf * kBK;
 constexpr uint32_t kTmemCols = 2 * kBN;
-// Epilogue staging: per promotion warp 32 rows x 128 BF16 columns as two
-// 32 x 64 boxes of 128-byte rows, 128-byte swizzled for the TMA store.
-constexpr uint32_t kEpiBoxBytes = 32 * 128;
+// Epilogue staging: a promotion warp writes its 32 rows x 128 BF16 columns
+// as four 32 x 32 boxes (64-byte rows, 64-byte swizzle) through two
+// alternating staging buffers, so rounding the next box overlaps the TMA
+// store reading the previous one.
+constexpr uint32_t kEpiBoxBytes = 32 * 64;
 constexpr uint32_t kEpiWarpBytes = 2 * kEpiBoxBytes;
 
 struct GemmParams {
     const float* sA;
     const float* sB;
-    uint16_t* D;          // [I][J] BF16 bit patterns
     int I, J, KC;         // output rows, output columns, reduction chunks
     int tiles_n;          // ceil(J / kBN)
-    int num_tiles;
+    int num_tiles;        // ceil(I / kPairM) * tiles_n
     uint64_t timeout_ns;
 };
 
+// One chunk's scales for one CTA: its 128 row scales and the tile's column
+// scales (Wgrad: 256 per-column values; Fprop/Dgrad: one per 128-column
+// block, b[0] and b[1]).
+struct alignas(16) ScaleSlot {
+    float a[128];
+    float b[256];
+};
+
 struct alignas(16) GemmCtl {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
-    uint64_t tfull[2];
-    uint64_t tempty[2];
+    uint64_t full[kStages];    // even CTA: both CTAs' bytes of the stage landed
+    uint64_t empty[kStages];   // both CTAs: the pair MMA has read the stage
+    uint64_t tfull[2];         // both CTAs: the chunk partial is in TMEM
+    uint64_t tempty[2];        // even CTA: both CTAs' promotion warps read it
+    uint64_t sfull[kScaleSlots];   // the slot's scale copies landed (32 producer lanes)
+    uint64_t sempty[kScaleSlots];  // the promotion warps are done with the slot (8 warps)
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
-    float sbw[kPromoWarps][2][128];  // Wgrad column scales: [warp][chunk parity][column]
+    uint32_t issued;           // loads this CTA's producer issued
+    uint32_t peer_issued;      // even CTA: loads the odd CTA's producer issued
+    ScaleSlot scl[kScaleSlots];
 };
+static_assert(offsetof(GemmCtl, scl) % 16 == 0, "scale slots are read with 16-byte vector loads");
 
 constexpr size_t kGemmSmemBytes =
     1024 + kStages * (kStageBytesA + kStageBytesB) + kPromoWarps * kEpiWarpBytes + sizeof(GemmCtl);
@@ -89,9 +123,11 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
 }
 
-__device__ __forceinline__ void raise_abort(GemmCtl* ctl, unsigned int* status) {
+// Stop both CTAs of the pair and record the timeout.
+__device__ __forceinline__ void raise_abort(GemmCtl* ctl, uint32_t peer_abort, unsigned int* status) {
     if ((threadIdx.x & 31) == 0) {
         ctl->abort = 1;
+        st_cluster_u32(peer_abort, 1u);
         atomicOr(status, 1u);
     }
 }
@@ -101,12 +137,23 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-template <int MODE>
-__device__ __forceinline__ float chunk_scale_b(const GemmParams& p, int c, int jh) {
-    if (MODE == kModeFprop) return __ldg(p.sB + static_cast<int64_t>(jh >> 7) * p.KC + c);
-    return __ldg(p.sB + static_cast<int64_t>(c) * (p.J >> 7) + (jh >> 7));
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
 
+__device__ __forceinline__ void cp_async_16g(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Arrive on `bar` once this thread's prior cp.async copies have landed
+// (counts against the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_drain() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Launched as clusters of two CTAs (grid = 2 x clusters).
 template <int MODE>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_block_scaled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -121,6 +168,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int first_tile = static_cast<int>(cluster_id_x());
+    const int tile_step = static_cast<int>(cluster_count_x());
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -129,27 +180,35 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&ctl->tfull[b], 1);
-            mbar_init(&ctl->tempty[b], kPromoWarps);
+            mbar_init(&ctl->tempty[b], 2 * kPromoWarps);
+        }
+        for (int q = 0; q < kScaleSlots; ++q) {
+            mbar_init(&ctl->sfull[q], 32);
+            mbar_init(&ctl->sempty[q], kPromoWarps);
         }
         mbar_init(&ctl->drain, 1);
         ctl->abort = 0;
+        ctl->issued = 0;
+        ctl->peer_issued = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
         tma_prefetch_desc(&tmD);
     }
     if (warp == 1) {
-        tmem_alloc(smem_addr(&ctl->tmem_base), kTmemCols);
-        tmem_relinquish();
+        tmem_alloc_pair(smem_addr(&ctl->tmem_base), kTmemCols);
+        tmem_relinquish_pair();
     }
+    // Both CTAs' barriers are initialised and the pair's TMEM is allocated
+    // before any copy, MMA or remote arrive targets them.
     tc_fence_before();
-    __syncthreads();
+    cluster_sync_all();
     tc_fence_after();
 
     const uint32_t tmem = ctl->tmem_base;
     volatile int* abort_flag = &ctl->abort;
+    const uint32_t peer_abort = mapa_shared(smem_addr(&ctl->abort), rank ^ 1u);
     const uint64_t lim = p.timeout_ns;
-    uint32_t producer_issued = 0;
 
     // Register split (launch: 384 x 168): warpgroup 0 keeps 40, the two
     // promotion warpgroups take 232 each; 128*40 + 256*232 == 384*168.
@@ -157,30 +216,57 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 40;" ::: "memory");
     if (warp == 0) {
         // ---------------------------------------------------------- producer
-        uint32_t s = 0, ph = 0, issued = 0;
+        const uint32_t full0 = mapa_shared(smem_addr(&ctl->full[0]), 0);
+        uint32_t s = 0, ph = 0, q = 0, qph = 0, issued = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+        for (int tile = first_tile; tile < p.num_tiles && ok; tile += tile_step) {
             const int tm = tile / p.tiles_n, tn = tile - tm * p.tiles_n;
+            const int r0 = tm * kPairM + static_cast<int>(rank) * kBM;  // this CTA's first row
+            const int j0 = tn * kBN;
             for (int c = 0; c < p.KC; ++c) {
+                // operands of chunk c
                 if (!warp_wait(&ctl->empty[s], ph ^ 1, abort_flag, lim)) { ok = false; break; }
                 if (lane == 0) {
-                    const uint32_t fb = smem_addr(&ctl->full[s]);
-                    mbar_arrive_expect_tx(&ctl->full[s], kStageBytesA + kStageBytesB);
-                    tma_load_2d(smem_addr(smA + s * kStageBytesA), &tmA, fb, c * kBK, tm * kBM);
-                    tma_load_2d(smem_addr(smB + s * kStageBytesB), &tmB, fb, c * kBK, tn * kBN);
+                    if (leader) mbar_arrive_expect_tx(&ctl->full[s], 2 * (kStageBytesA + kStageBytesB));
+                    const uint32_t fb = full0 + s * 8;
+                    tma_load_2d_pair(smem_addr(smA + s * kStageBytesA), &tmA, fb, c * kBK, r0);
+                    tma_load_2d_pair(smem_addr(smB + s * kStageBytesB), &tmB, fb, c * kBK,
+                                     j0 + static_cast<int>(rank) * kBNHalf);
                 }
                 ++issued;
                 if (++s == kStages) { s = 0; ph ^= 1; }
+                // scales of chunk c (rows and columns past the problem are skipped)
+                if (!warp_wait(&ctl->sempty[q], qph ^ 1, abort_flag, lim)) { ok = false; break; }
+                ScaleSlot& sl = ctl->scl[q];
+                if (r0 < p.I) cp_async_16g(smem_addr(&sl.a[4 * lane]), p.sA + static_cast<int64_t>(c) * p.I + r0 + 4 * lane);
+                if (MODE == kModeWgrad) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int j = j0 + h * 128 + 4 * lane;
+                        if (j < p.J)
+                            cp_async_16g(smem_addr(&sl.b[h * 128 + 4 * lane]), p.sB + static_cast<int64_t>(c) * p.J + j);
+                    }
+                } else if (lane < 2) {
+                    const int jb = (j0 >> 7) + lane;  // 128-column block of the weight
+                    if (jb * 128 < p.J) {
+                        const float* src = MODE == kModeFprop ? p.sB + static_cast<int64_t>(jb) * p.KC + c
+                                                              : p.sB + static_cast<int64_t>(c) * (p.J >> 7) + jb;
+                        cp_async_4(smem_addr(&sl.b[lane]), src);
+                    }
+                }
+                cp_async_arrive(&ctl->sfull[q]);
+                if (++q == kScaleSlots) { q = 0; qph ^= 1; }
             }
         }
-        if (!ok) raise_abort(ctl, status);
-        producer_issued = issued;
-    } else if (warp == 1) {
+        cp_async_drain();
+        if (!ok) raise_abort(ctl, peer_abort, status);
+        if (lane == 0) ctl->issued = issued;
+    } else if (warp == 1 && leader) {
         // --------------------------------------------------------------- MMA
-        constexpr uint32_t idesc = idesc_e4m3_f32(kBM, kBN);
+        constexpr uint32_t idesc = idesc_e4m3_f32(kPairM, kBN);
         uint32_t s = 0, ph = 0, buf = 0, tph = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+        for (int tile = first_tile; tile < p.num_tiles && ok; tile += tile_step) {
             for (int c = 0; c < p.KC; ++c) {
                 if (!warp_wait(&ctl->tempty[buf], tph ^ 1, abort_flag, lim)) { ok = false; break; }
                 if (!warp_wait(&ctl->full[s], ph, abort_flag, lim)) { ok = false; break; }
@@ -191,9 +277,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const uint32_t d = tmem + buf * kBN;
 #pragma unroll
                     for (int k = 0; k < kBK / 32; ++k)
-                        mma_e4m3(d, sw128_kmajor_desc(a0 + 32 * k), sw128_kmajor_desc(b0 + 32 * k), idesc, k > 0);
-                    mma_commit(smem_addr(&ctl->empty[s]));
-                    mma_commit(smem_addr(&ctl->tfull[buf]));
+                        mma_e4m3_pair(d, sw128_kmajor_desc(a0 + 32 * k), sw128_kmajor_desc(b0 + 32 * k), idesc,
+                                      k > 0);
+                    mma_commit_pair_mc(smem_addr(&ctl->empty[s]), 0x3);
+                    mma_commit_pair_mc(smem_addr(&ctl->tfull[buf]), 0x3);
                 }
                 __syncwarp();
                 if (++s == kStages) { s = 0; ph ^= 1; }
@@ -201,7 +288,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 if (buf == 0) tph ^= 1;
             }
         }
-        if (!ok) raise_abort(ctl, status);
+        if (!ok) raise_abort(ctl, peer_abort, status);
     }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 232;" ::: "memory");
@@ -211,74 +298,72 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int half = pw >> 2;              // which 128 columns of the tile
         const int row = quarter * 32 + lane;   // tile row == TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        uint32_t buf = 0, tph = 0, it = 0;
+        const uint32_t tempty0 = mapa_shared(smem_addr(&ctl->tempty[0]), 0);
+        uint32_t buf = 0, tph = 0, q = 0, qph = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+        for (int tile = first_tile; tile < p.num_tiles && ok; tile += tile_step) {
             const int tm = tile / p.tiles_n, tn = tile - tm * p.tiles_n;
-            const int gi = tm * kBM + row;
+            const int r0 = tm * kPairM + static_cast<int>(rank) * kBM;  // first row of this CTA's half
+            const bool rv = r0 < p.I;
             const int jh = tn * kBN + half * 128;
             const bool hv = jh < p.J;
             float acc[128];
 #pragma unroll
             for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
 
-            for (int c = 0; c < p.KC; ++c, ++it) {
-                const float sa = __ldg(p.sA + static_cast<int64_t>(c) * p.I + gi);
-                float sb = 0.0f;
-                if (MODE != kModeWgrad) {
-                    sb = hv ? chunk_scale_b<MODE>(p, c, jh) : 0.0f;
-                } else {
-                    // each warp stages its own copy of the 128 column scales
-                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (hv) v = __ldg(reinterpret_cast<const float4*>(p.sB + static_cast<int64_t>(c) * p.J + jh) + lane);
-                    reinterpret_cast<float4*>(ctl->sbw[pw][it & 1])[lane] = v;
-                    __syncwarp();
-                }
+            for (int c = 0; c < p.KC; ++c) {
+                if (!warp_wait(&ctl->sfull[q], qph, abort_flag, lim)) { ok = false; break; }
+                const ScaleSlot& sl = ctl->scl[q];
+                const float sa = sl.a[row];
+                const float sab = MODE == kModeWgrad ? 0.0f : sa * sl.b[half];
+                const float* sbs = &sl.b[half * 128];   // Wgrad column scales of this half
                 if (!warp_wait(&ctl->tfull[buf], tph, abort_flag, lim)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t tbase = tmem + lane_off + buf * kBN + half * 128;
-                if (MODE != kModeWgrad) {
-                    // acc += (sA * sB) * partial, two columns per packed FMA
-                    const float sab = sa * sb;
+                // acc += (sA * sB) * partial (Fprop, Dgrad), or
+                // acc += sA * (sB[j] * partial) (Wgrad), 32 columns at a time.
+                auto promote = [&](const uint32_t (&v)[32], int g) {
+                    float* a = acc + g * 32;
+                    if (MODE != kModeWgrad) {
 #pragma unroll
-                    for (int g = 0; g < 2; ++g) {
-                        uint32_t r0[32], r1[32];
-                        tmem_ld_32x32b_x32(tbase + g * 64, r0);
-                        tmem_ld_32x32b_x32(tbase + g * 64 + 32, r1);
-                        tmem_wait_ld();
-                        reg_fence32(r0);
-                        reg_fence32(r1);
-                        float* a = acc + g * 64;
-#pragma unroll
-                        for (int i = 0; i < 32; i += 2) {
-                            ffma2(a[i], a[i + 1], sab, sab, __uint_as_float(r0[i]), __uint_as_float(r0[i + 1]));
-                            ffma2(a[32 + i], a[33 + i], sab, sab, __uint_as_float(r1[i]), __uint_as_float(r1[i + 1]));
-                        }
-                    }
-                } else {
-                    // per-column scales: acc += sA * (sB[j] * partial)
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        uint32_t r0[32];
-                        tmem_ld_32x32b_x32(tbase + g * 32, r0);
-                        tmem_wait_ld();
-                        reg_fence32(r0);
-                        const float* sbv = &ctl->sbw[pw][it & 1][g * 32];
-                        float* a = acc + g * 32;
+                        for (int i = 0; i < 32; ++i) a[i] = __fmaf_rn(sab, __uint_as_float(v[i]), a[i]);
+                    } else {
 #pragma unroll
                         for (int i = 0; i < 32; i += 4) {
-                            const float4 b = *reinterpret_cast<const float4*>(sbv + i);
+                            const float4 b = *reinterpret_cast<const float4*>(sbs + g * 32 + i);
                             float t0, t1, t2, t3;
-                            fmul2(t0, t1, __uint_as_float(r0[i]), __uint_as_float(r0[i + 1]), b.x, b.y);
-                            fmul2(t2, t3, __uint_as_float(r0[i + 2]), __uint_as_float(r0[i + 3]), b.z, b.w);
+                            fmul2(t0, t1, __uint_as_float(v[i]), __uint_as_float(v[i + 1]), b.x, b.y);
+                            fmul2(t2, t3, __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]), b.z, b.w);
                             ffma2(a[i], a[i + 1], t0, t1, sa, sa);
                             ffma2(a[i + 2], a[i + 3], t2, t3, sa, sa);
                         }
                     }
-                }
+                };
+                // Two 32-column staging buffers: groups 0 and 1 load together,
+                // group 2 loads while group 0 is multiplied in, group 3 while
+                // group 1 is; the TMEM buffer goes back to the MMA as soon as
+                // group 3 is in registers.
+                uint32_t ra[32], rb[32];
+                tmem_ld_32x32b_x32(tbase, ra);
+                tmem_ld_32x32b_x32(tbase + 32, rb);
+                tmem_wait_ld();
+                reg_fence32(ra);
+                reg_fence32(rb);
+                promote(ra, 0);
+                tmem_ld_32x32b_x32(tbase + 64, ra);
+                promote(rb, 1);
+                tmem_ld_32x32b_x32(tbase + 96, rb);
+                tmem_wait_ld();
+                reg_fence32(ra);
+                reg_fence32(rb);
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&ctl->tempty[buf]);
+                if (lane == 0) mbar_arrive_cluster(tempty0 + buf * 8);
+                promote(ra, 2);
+                promote(rb, 3);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->sempty[q]);
+                if (++q == kScaleSlots) { q = 0; qph ^= 1; }
                 buf ^= 1;
                 if (buf == 0) tph ^= 1;
             }
@@ -287,55 +372,62 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             // then one lane issues the TMA stores (asynchronous: they drain
             // while the next tile's chunks are promoted).
             uint8_t* stg = smEpi + pw * kEpiWarpBytes;
-            if (lane == 0) bulk_wait_group_read<0>();  // the previous tile's stores left the buffer
-            __syncwarp();
+            const int y0 = r0 + quarter * 32;
+            const bool store = hv && rv;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int bx = 0; bx < 4; ++bx) {
+                uint8_t* box = stg + (bx & 1) * kEpiBoxBytes;
+                // the store issued from this buffer two boxes ago has read it
+                if (lane == 0) bulk_wait_group_read<1>();
+                __syncwarp();
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float* a = acc + h * 64 + j * 8;
+                for (int j = 0; j < 4; ++j) {
+                    const float* a = acc + bx * 32 + j * 8;
                     uint4 o;
                     o.x = pack_bf16x2(a[0], a[1]);
                     o.y = pack_bf16x2(a[2], a[3]);
                     o.z = pack_bf16x2(a[4], a[5]);
                     o.w = pack_bf16x2(a[6], a[7]);
-                    *reinterpret_cast<uint4*>(stg + h * kEpiBoxBytes + lane * 128 + ((j ^ (lane & 7)) << 4)) = o;
+                    // 64-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ ((r >> 1) & 3)
+                    *reinterpret_cast<uint4*>(box + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) = o;
                 }
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0 && hv) {
-                const int y0 = tm * kBM + quarter * 32;
-                tma_store_2d(&tmD, smem_addr(stg), jh, y0);
-                tma_store_2d(&tmD, smem_addr(stg + kEpiBoxBytes), jh + 64, y0);
-                bulk_commit_group();
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (store) tma_store_2d(&tmD, smem_addr(box), jh + bx * 32, y0);
+                    bulk_commit_group();
+                }
             }
         }
         if (lane == 0) bulk_wait_group<0>();  // all output writes complete before exit
-        if (!ok) raise_abort(ctl, status);
+        if (!ok) raise_abort(ctl, peer_abort, status);
     }
 
-    // Teardown.  Every role has stopped (all waits are bounded).  After an
-    // abort, let this CTA's own in-flight copies land and its MMAs finish
-    // before shared memory and TMEM are released.
+    // Teardown.  Every role has stopped (all waits are bounded).  The odd CTA
+    // reports how many loads its producer issued; after an abort the even CTA
+    // waits (bounded) for every copy either producer issued and for its own
+    // in-flight MMAs, which read both CTAs' shared memory and write both
+    // CTAs' TMEM, before either CTA frees TMEM or exits.
     tc_fence_before();
     __syncthreads();
-    if (*abort_flag) {
+    if (!leader && threadIdx.x == 0) st_cluster_u32(mapa_shared(smem_addr(&ctl->peer_issued), 0), ctl->issued);
+    cluster_sync_all();
+    if (leader && *abort_flag) {
         if (warp == 0 && lane == 0) {
-            const uint32_t n = producer_issued < kStages ? producer_issued : kStages;
-            for (uint32_t i = 0; i < n; ++i) {
-                const uint32_t f = producer_issued - 1 - i;
+            const uint32_t n = ctl->issued > ctl->peer_issued ? ctl->issued : ctl->peer_issued;
+            const uint32_t f0 = n > static_cast<uint32_t>(kStages) ? n - kStages : 0;
+            for (uint32_t f = f0; f < n; ++f)
                 bounded_wait(&ctl->full[f % kStages], (f / kStages) & 1, nullptr, lim);
-            }
         }
         if (warp == 1 && lane == 0) {
-            mma_commit(smem_addr(&ctl->drain));
+            mma_commit_pair(smem_addr(&ctl->drain));
             bounded_wait(&ctl->drain, 0, nullptr, lim);
         }
-        __syncthreads();
     }
+    tc_fence_before();
+    cluster_sync_all();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+    if (warp == 1) tmem_dealloc_pair(tmem, kTmemCols);
 }
 
 // Self-test of the bounded wait: one CTA waits on a barrier that nothing will
