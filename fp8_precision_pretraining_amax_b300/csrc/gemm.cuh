@@ -15,21 +15,26 @@
 // threads each, one 256 x 256 output tile per cluster at a time, K chunk of
 // 128 (one scale chunk).  CTA rank r of the pair owns output rows
 // [128 r, 128 r + 128) of the tile and all 256 columns.
-//   warp 0      producer (both CTAs): TMA loads of this CTA's 128 rows of A
-//               and its half (128 rows) of B per chunk into a 5-stage
-//               shared-memory ring (128-byte swizzle), completion bytes
-//               counted on the even CTA's full barrier, which expects both
-//               CTAs' bytes; and cp.async copies of the chunk's scales (this
-//               CTA's 128 row scales and the tile's column scales) into an
-//               8-slot scale ring, so no promotion warp ever waits on a
-//               global-memory load.
+//   warp 0      operand producer (both CTAs): TMA loads of this CTA's 128
+//               rows of A and its half (128 rows) of B per chunk into a
+//               6-stage shared-memory ring (128-byte swizzle), completion
+//               bytes counted on the even CTA's full barrier, which expects
+//               both CTAs' bytes.
+//   warp 2      scale producer (both CTAs): cp.async copies of each chunk's
+//               scales (this CTA's 128 row scales and the tile's column
+//               scales) into a 6-slot ring, so no promotion warp ever waits
+//               on a global-memory load.
 //   warp 1      allocates the pair's TMEM (both CTAs); in the even CTA one
 //               thread issues four tcgen05.mma.cta_group::2.kind::f8f6f4
 //               (256x256x32) per chunk into one of two TMEM partial buffers
 //               of 256 FP32 columns, started fresh every chunk, then commits
-//               with a multicast to both CTAs' stage-empty and partial-full
-//               barriers.
-//   warps 2, 3  idle (the first warpgroup gives up registers: 40 per thread)
+//               with a multicast to both CTAs' partial-full barriers.  The
+//               completed partial also means the stage was read: in Fprop and
+//               Dgrad the first promotion warp of each CTA then frees the
+//               stage for its producer, keeping one commit off the MMA
+//               thread's critical path; in Wgrad (promotion-bound) the MMA
+//               commits to the stage-empty barriers as well.
+//   warp 3      idle (the first warpgroup gives up registers: 40 per thread)
 //   warps 4..11 promotion (two warpgroups at 232 registers per thread, both
 //               CTAs): each thread owns one output row and 128 columns; it
 //               reads the chunk partial from its CTA's TMEM (tcgen05.ld),
@@ -64,8 +69,8 @@ constexpr int kPairM = 256;       // tile rows per CTA pair
 constexpr int kBN = 256;          // tile columns (MMA N)
 constexpr int kBNHalf = 128;      // B rows each CTA loads
 constexpr int kBK = 128;          // one scale chunk of the reduction
-constexpr int kStages = 5;
-constexpr int kScaleSlots = 8;
+constexpr int kStages = 6;
+constexpr int kScaleSlots = 6;
 constexpr int kGemmThreads = 384;
 constexpr int kFirstPromoWarp = 4;
 constexpr int kPromoWarps = 8;
@@ -73,11 +78,10 @@ constexpr uint32_t kStageBytesA = kBM * kBK;
 constexpr uint32_t kStageBytesB = kBNHalf * kBK;
 constexpr uint32_t kTmemCols = 2 * kBN;
 // Epilogue staging: a promotion warp writes its 32 rows x 128 BF16 columns
-// as four 32 x 32 boxes (64-byte rows, 64-byte swizzle) through two
-// alternating staging buffers, so rounding the next box overlaps the TMA
-// store reading the previous one.
+// as four 32 x 32 boxes (64-byte rows, 64-byte swizzle) through one 2 KB
+// staging buffer (shared memory goes to the operand ring instead).
 constexpr uint32_t kEpiBoxBytes = 32 * 64;
-constexpr uint32_t kEpiWarpBytes = 2 * kEpiBoxBytes;
+constexpr uint32_t kEpiWarpBytes = kEpiBoxBytes;
 
 struct GemmParams {
     const float* sA;
@@ -98,7 +102,7 @@ struct alignas(16) ScaleSlot {
 
 struct alignas(16) GemmCtl {
     uint64_t full[kStages];    // even CTA: both CTAs' bytes of the stage landed
-    uint64_t empty[kStages];   // both CTAs: the pair MMA has read the stage
+    uint64_t empty[kStages];   // both CTAs: the pair MMA has read the stage (signalled by promotion warp 0)
     uint64_t tfull[2];         // both CTAs: the chunk partial is in TMEM
     uint64_t tempty[2];        // even CTA: both CTAs' promotion warps read it
     uint64_t sfull[kScaleSlots];   // the slot's scale copies landed (32 producer lanes)
@@ -114,6 +118,7 @@ static_assert(offsetof(GemmCtl, scl) % 16 == 0, "scale slots are read with 16-by
 
 constexpr size_t kGemmSmemBytes =
     1024 + kStages * (kStageBytesA + kStageBytesB) + kPromoWarps * kEpiWarpBytes + sizeof(GemmCtl);
+static_assert(kGemmSmemBytes <= 232448, "more dynamic shared memory than one sm_103 CTA can have");
 
 // One lane waits, the verdict is broadcast so the warp stays converged.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
@@ -209,36 +214,52 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     volatile int* abort_flag = &ctl->abort;
     const uint32_t peer_abort = mapa_shared(smem_addr(&ctl->abort), rank ^ 1u);
     const uint64_t lim = p.timeout_ns;
+    constexpr bool kStageFreedByMma = MODE == kModeWgrad;
 
     // Register split (launch: 384 x 168): warpgroup 0 keeps 40, the two
     // promotion warpgroups take 232 each; 128*40 + 256*232 == 384*168.
     if (warp < kFirstPromoWarp) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 40;" ::: "memory");
     if (warp == 0) {
-        // ---------------------------------------------------------- producer
+        // ------------------------------------------------- operand producer
         const uint32_t full0 = mapa_shared(smem_addr(&ctl->full[0]), 0);
-        uint32_t s = 0, ph = 0, q = 0, qph = 0, issued = 0;
+        uint32_t s = 0, ph = 0, issued = 0;
         bool ok = true;
         for (int tile = first_tile; tile < p.num_tiles && ok; tile += tile_step) {
             const int tm = tile / p.tiles_n, tn = tile - tm * p.tiles_n;
             const int r0 = tm * kPairM + static_cast<int>(rank) * kBM;  // this CTA's first row
-            const int j0 = tn * kBN;
+            const int b0 = tn * kBN + static_cast<int>(rank) * kBNHalf;  // this CTA's first B row
             for (int c = 0; c < p.KC; ++c) {
-                // operands of chunk c
                 if (!warp_wait(&ctl->empty[s], ph ^ 1, abort_flag, lim)) { ok = false; break; }
                 if (lane == 0) {
                     if (leader) mbar_arrive_expect_tx(&ctl->full[s], 2 * (kStageBytesA + kStageBytesB));
                     const uint32_t fb = full0 + s * 8;
                     tma_load_2d_pair(smem_addr(smA + s * kStageBytesA), &tmA, fb, c * kBK, r0);
-                    tma_load_2d_pair(smem_addr(smB + s * kStageBytesB), &tmB, fb, c * kBK,
-                                     j0 + static_cast<int>(rank) * kBNHalf);
+                    tma_load_2d_pair(smem_addr(smB + s * kStageBytesB), &tmB, fb, c * kBK, b0);
                 }
                 ++issued;
                 if (++s == kStages) { s = 0; ph ^= 1; }
-                // scales of chunk c (rows and columns past the problem are skipped)
+            }
+        }
+        if (!ok) raise_abort(ctl, peer_abort, status);
+        if (lane == 0) ctl->issued = issued;
+    } else if (warp == 2) {
+        // --------------------------------------------------- scale producer
+        // Copies each chunk's scales into the next ring slot: this CTA's 128
+        // row scales, and the tile's column scales (Wgrad: 256 values;
+        // Fprop/Dgrad: the weight-block scale of each 128-column half).
+        // Rows and columns past the problem are skipped.
+        uint32_t q = 0, qph = 0;
+        bool ok = true;
+        for (int tile = first_tile; tile < p.num_tiles && ok; tile += tile_step) {
+            const int tm = tile / p.tiles_n, tn = tile - tm * p.tiles_n;
+            const int r0 = tm * kPairM + static_cast<int>(rank) * kBM;
+            const int j0 = tn * kBN;
+            for (int c = 0; c < p.KC; ++c) {
                 if (!warp_wait(&ctl->sempty[q], qph ^ 1, abort_flag, lim)) { ok = false; break; }
                 ScaleSlot& sl = ctl->scl[q];
-                if (r0 < p.I) cp_async_16g(smem_addr(&sl.a[4 * lane]), p.sA + static_cast<int64_t>(c) * p.I + r0 + 4 * lane);
+                if (r0 < p.I)
+                    cp_async_16g(smem_addr(&sl.a[4 * lane]), p.sA + static_cast<int64_t>(c) * p.I + r0 + 4 * lane);
                 if (MODE == kModeWgrad) {
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
@@ -260,18 +281,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         cp_async_drain();
         if (!ok) raise_abort(ctl, peer_abort, status);
-        if (lane == 0) ctl->issued = issued;
     } else if (warp == 1 && leader) {
         // --------------------------------------------------------------- MMA
-        constexpr uint32_t idesc = idesc_e4m3_f32(kPairM, kBN);
-        uint32_t s = 0, ph = 0, buf = 0, tph = 0;
+        // One thread runs the whole loop (no per-wait warp broadcast).
         bool ok = true;
-        for (int tile = first_tile; tile < p.num_tiles && ok; tile += tile_step) {
-            for (int c = 0; c < p.KC; ++c) {
-                if (!warp_wait(&ctl->tempty[buf], tph ^ 1, abort_flag, lim)) { ok = false; break; }
-                if (!warp_wait(&ctl->full[s], ph, abort_flag, lim)) { ok = false; break; }
-                tc_fence_after();
-                if (lane == 0) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_e4m3_f32(kPairM, kBN);
+            uint32_t s = 0, ph = 0, buf = 0, tph = 0;
+            for (int tile = first_tile; tile < p.num_tiles && ok; tile += tile_step) {
+                for (int c = 0; c < p.KC; ++c) {
+                    // the long wait suspends (try_wait) so it takes no issue slots
+                    // from the promotion warps sharing this SM sub-partition
+                    if (!bounded_wait(&ctl->tempty[buf], tph ^ 1, abort_flag, lim)) { ok = false; break; }
+                    if (!bounded_spin(&ctl->full[s], ph, abort_flag, lim)) { ok = false; break; }
+                    tc_fence_after();
                     const uint32_t a0 = smem_addr(smA + s * kStageBytesA);
                     const uint32_t b0 = smem_addr(smB + s * kStageBytesB);
                     const uint32_t d = tmem + buf * kBN;
@@ -279,15 +302,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     for (int k = 0; k < kBK / 32; ++k)
                         mma_e4m3_pair(d, sw128_kmajor_desc(a0 + 32 * k), sw128_kmajor_desc(b0 + 32 * k), idesc,
                                       k > 0);
-                    mma_commit_pair_mc(smem_addr(&ctl->empty[s]), 0x3);
+                    // Fprop/Dgrad: one commit per chunk (the completed partial
+                    // also means the stage was read; a promotion warp hands the
+                    // stage back).  Wgrad, whose promotion is the slower side,
+                    // frees the stage from the MMA itself.
+                    if (kStageFreedByMma) mma_commit_pair_mc(smem_addr(&ctl->empty[s]), 0x3);
                     mma_commit_pair_mc(smem_addr(&ctl->tfull[buf]), 0x3);
+                    if (++s == kStages) { s = 0; ph ^= 1; }
+                    buf ^= 1;
+                    if (buf == 0) tph ^= 1;
                 }
-                __syncwarp();
-                if (++s == kStages) { s = 0; ph ^= 1; }
-                buf ^= 1;
-                if (buf == 0) tph ^= 1;
             }
         }
+        __syncwarp();
+        ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
         if (!ok) raise_abort(ctl, peer_abort, status);
     }
     } else {
@@ -299,7 +327,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int row = quarter * 32 + lane;   // tile row == TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t tempty0 = mapa_shared(smem_addr(&ctl->tempty[0]), 0);
-        uint32_t buf = 0, tph = 0, q = 0, qph = 0;
+        uint32_t buf = 0, tph = 0, q = 0, qph = 0, stage = 0;
         bool ok = true;
         for (int tile = first_tile; tile < p.num_tiles && ok; tile += tile_step) {
             const int tm = tile / p.tiles_n, tn = tile - tm * p.tiles_n;
@@ -318,6 +346,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const float sab = MODE == kModeWgrad ? 0.0f : sa * sl.b[half];
                 const float* sbs = &sl.b[half * 128];   // Wgrad column scales of this half
                 if (!warp_wait(&ctl->tfull[buf], tph, abort_flag, lim)) { ok = false; break; }
+                // the MMA that produced this partial has read the chunk's
+                // operand stage: this CTA's producer may refill it
+                if (!kStageFreedByMma && pw == 0 && lane == 0) mbar_arrive(&ctl->empty[stage]);
+                if (++stage == kStages) stage = 0;
                 tc_fence_after();
                 const uint32_t tbase = tmem + lane_off + buf * kBN + half * 128;
                 // acc += (sA * sB) * partial (Fprop, Dgrad), or
@@ -376,9 +408,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const bool store = hv && rv;
 #pragma unroll
             for (int bx = 0; bx < 4; ++bx) {
-                uint8_t* box = stg + (bx & 1) * kEpiBoxBytes;
-                // the store issued from this buffer two boxes ago has read it
-                if (lane == 0) bulk_wait_group_read<1>();
+                uint8_t* box = stg;
+                // the previous box's store has finished reading the buffer
+                if (lane == 0) bulk_wait_group_read<0>();
                 __syncwarp();
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
