@@ -290,10 +290,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t s = 0, ph = 0, buf = 0, tph = 0;
             for (int tile = first_tile; tile < p.num_tiles && ok; tile += tile_step) {
                 for (int c = 0; c < p.KC; ++c) {
-                    // the long wait suspends (try_wait) so it takes no issue slots
-                    // from the promotion warps sharing this SM sub-partition
+                    // Both waits suspend (try_wait): this thread shares its SM
+                    // sub-partition with two promotion warps (TMEM lanes 32-63),
+                    // the last to hand the partial buffer back, so it must not
+                    // take their issue slots by spinning.
                     if (!bounded_wait(&ctl->tempty[buf], tph ^ 1, abort_flag, lim)) { ok = false; break; }
-                    if (!bounded_spin(&ctl->full[s], ph, abort_flag, lim)) { ok = false; break; }
+                    if (!bounded_wait(&ctl->full[s], ph, abort_flag, lim)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t a0 = smem_addr(smA + s * kStageBytesA);
                     const uint32_t b0 = smem_addr(smB + s * kStageBytesB);
