@@ -25,11 +25,11 @@ end to end through the Python API with pinned host buffers (host->device
 copies of X, W, dY and device->host copies of Y, dX, dW inside the timed
 region), and the CPU oracle timed on a bounded sample on the host cores.
 
-Multi-GPU (torchrun): every rank runs its own replica of the workload (the
-linears shard over tokens with no exchange for Fprop/Dgrad; a data-parallel
-Wgrad all-reduce belongs to the optimizer step, outside this path), so
-scaling is weak; the timed region is bracketed by barriers and the max over
-ranks is reported.
+Multi-GPU (torchrun): data parallel with weak scaling.  Every rank runs the
+step on its own batch of the workload's size; Fprop and Dgrad need nothing
+from other ranks, and the dW of every linear is summed over the ranks with an
+NCCL all-reduce inside the timed step (the only exchange of the path).  The
+timed region is bracketed by barriers and the max over ranks is reported.
 """
 from __future__ import annotations
 
@@ -240,9 +240,15 @@ def run_ours(args, rank, world, local_rank):
     lins = make_inputs(args.workload, dev, args.tokens)
     layers = [LinearFP8(l.M, l.K, l.N, device=dev) for l in lins]
     plan = [step_launches(fp8bq, L, lin) for L, lin in zip(layers, lins)]
+    if world > 1:
+        # data parallel: each rank's batch gives a partial dW; the ranks sum
+        # them (NCCL all-reduce of the BF16 dW of every linear, each step)
+        for L, launches in zip(layers, plan):
+            launches.append(("comm_allreduce_dw", 2 * L.N * L.K,
+                             lambda L=L: torch.distributed.all_reduce(L.dw, op=torch.distributed.ReduceOp.SUM)))
     torch.cuda.synchronize()
     flops = step_flops(shapes)
-    launches_per_step = sum(len(p) for p in plan)
+    launches_per_step = sum(1 for p in plan for kind, _, _ in p if not kind.startswith("comm"))
 
     def barrier():
         if world > 1:
@@ -331,7 +337,8 @@ def run_ours(args, rank, world, local_rank):
                                "frac_of_hbm": q_by / (q_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
                                "ms_per_step": q_ms / args.steps}
     cfg = workload_config(args.workload, args.tokens)
-    cfg["parallelism"] = f"replicas x{world}" if world > 1 else "single GPU"
+    cfg["parallelism"] = (f"data parallel x{world}: own batch per rank, dW all-reduced each step"
+                          if world > 1 else "single GPU")
     cfg["l2"] = "inputs larger than L2 (no flush)" if args.workload != "tiny" else "inputs fit in L2"
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -375,6 +382,8 @@ def run_e2e(args, lins, layers, dev, flops, world, barrier):
             dw_.copy_(hw, non_blocking=True)
             ddy.copy_(hdy, non_blocking=True)
             L.step(dx_, dw_, ddy)
+            if world > 1:
+                torch.distributed.all_reduce(L.dw, op=torch.distributed.ReduceOp.SUM)
             oy.copy_(L.y, non_blocking=True)
             odx.copy_(L.dx, non_blocking=True)
             odw.copy_(L.dw, non_blocking=True)

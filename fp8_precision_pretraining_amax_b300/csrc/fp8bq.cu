@@ -138,15 +138,16 @@ int encode_u8_map(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t ou
     return r == CUDA_SUCCESS ? FP8BQ_OK : FP8BQ_ERR_CUDA;
 }
 
-// 2-D BF16 output [rows][cols] (dense), store boxes of 32 rows x 32 columns
-// (64-byte rows) with 64-byte swizzle, matching the epilogue staging.
-int encode_bf16_out_map(CUtensorMap* map, void* ptr, uint64_t cols, uint64_t rows) {
+// 2-D output [rows][cols] (dense), BF16 or FP32, store boxes of 32 rows x
+// 64 bytes (32 BF16 or 16 FP32 columns) with 64-byte swizzle, matching the
+// epilogue staging.
+int encode_out_map(CUtensorMap* map, void* ptr, uint64_t cols, uint64_t rows, bool f32) {
     const cuuint64_t dims[2] = {cols, rows};
-    const cuuint64_t strides[1] = {cols * 2};
-    const cuuint32_t box[2] = {32, 32};
+    const cuuint64_t strides[1] = {cols * (f32 ? 4 : 2)};
+    const cuuint32_t box[2] = {f32 ? 16u : 32u, 32};
     const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides, box, estr,
-                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+    const CUresult r = g_encode(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr,
+                                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? FP8BQ_OK : FP8BQ_ERR_CUDA;
 }
@@ -165,9 +166,10 @@ int launch_tile(const void* x, int dtype, int64_t R, int64_t C, int64_t ldx, uin
     return launch_status();
 }
 
+// D is BF16 (out_f32 = false) or FP32; accumulate (FP32 only) adds into D.
 template <int MODE>
-int run_gemm(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, uint16_t* D, int64_t I,
-             int64_t J, int64_t Kr, cudaStream_t stream) {
+int run_gemm(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, void* D, int64_t I,
+             int64_t J, int64_t Kr, cudaStream_t stream, bool out_f32 = false, bool accumulate = false) {
     if (I < 0 || J < 0 || Kr < 0) return FP8BQ_ERR_SHAPE;
     if ((I % 128) || (J % 128) || (Kr % 128)) return FP8BQ_ERR_SHAPE;
     if (I >= (int64_t(1) << 31) || J >= (int64_t(1) << 31) || Kr >= (int64_t(1) << 31)) return FP8BQ_ERR_SHAPE;
@@ -180,15 +182,17 @@ int run_gemm(const uint8_t* A, const float* sA, const uint8_t* B, const float* s
     int st = probe_device(&dev);
     if (st != FP8BQ_OK) return st;
     if (Kr == 0) {
-        // empty reduction: the product is exactly zero
-        return cudaMemsetAsync(D, 0, static_cast<size_t>(I) * J * 2, stream) == cudaSuccess ? FP8BQ_OK
-                                                                                            : FP8BQ_ERR_CUDA;
+        // empty reduction: the product is exactly zero (adding it changes nothing)
+        if (accumulate) return FP8BQ_OK;
+        return cudaMemsetAsync(D, 0, static_cast<size_t>(I) * J * (out_f32 ? 4 : 2), stream) == cudaSuccess
+                   ? FP8BQ_OK
+                   : FP8BQ_ERR_CUDA;
     }
 
     CUtensorMap ta, tb, td;
     if (encode_u8_map(&ta, A, Kr, I, fp8bq::kBM) != FP8BQ_OK) return FP8BQ_ERR_CUDA;
     if (encode_u8_map(&tb, B, Kr, J, fp8bq::kBNHalf) != FP8BQ_OK) return FP8BQ_ERR_CUDA;
-    if (encode_bf16_out_map(&td, D, J, I) != FP8BQ_OK) return FP8BQ_ERR_CUDA;
+    if (encode_out_map(&td, D, J, I, out_f32) != FP8BQ_OK) return FP8BQ_ERR_CUDA;
 
     fp8bq::GemmParams p;
     p.sA = sA;
@@ -200,6 +204,8 @@ int run_gemm(const uint8_t* A, const float* sA, const uint8_t* B, const float* s
     const int64_t tiles = ((I + fp8bq::kPairM - 1) / fp8bq::kPairM) * p.tiles_n;
     if (tiles >= (int64_t(1) << 31)) return FP8BQ_ERR_SHAPE;
     p.num_tiles = static_cast<int>(tiles);
+    p.out_f32 = out_f32 ? 1 : 0;
+    p.accumulate = accumulate ? 1 : 0;
     p.timeout_ns = kDefaultTimeoutNs;
     // persistent: one CTA pair per TPC that can hold one, never more pairs than tiles
     const int pairs = static_cast<int>(tiles < dev->max_pairs ? tiles : dev->max_pairs);
@@ -298,6 +304,13 @@ int fp8bq_gemm_dgrad(const uint8_t* dyq, const float* sdy, const uint8_t* wqT, c
 int fp8bq_gemm_wgrad(const uint8_t* dyqT, const float* sdyT, const uint8_t* xqT, const float* sxT, uint16_t* dw,
                      int64_t M, int64_t N, int64_t K, fp8bq_stream_t stream) {
     return run_gemm<fp8bq::kModeWgrad>(dyqT, sdyT, xqT, sxT, dw, N, K, M, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fp8bq_gemm_wgrad_f32(const uint8_t* dyqT, const float* sdyT, const uint8_t* xqT, const float* sxT, float* dw,
+                         int64_t M, int64_t N, int64_t K, int accumulate, fp8bq_stream_t stream) {
+    if (accumulate != 0 && accumulate != 1) return FP8BQ_ERR_SHAPE;
+    return run_gemm<fp8bq::kModeWgrad>(dyqT, sdyT, xqT, sxT, dw, N, K, M, reinterpret_cast<cudaStream_t>(stream),
+                                       true, accumulate == 1);
 }
 
 int fp8bq_check(fp8bq_stream_t stream) {

@@ -44,7 +44,8 @@
 //               chunk's scale product into FP32 accumulators.  While it does
 //               so the tensor cores already compute the next chunk into the
 //               other buffer.  After the last chunk the accumulators are
-//               rounded to BF16 and stored with TMA.
+//               rounded to BF16 (or kept in FP32 and optionally added into
+//               the output with a TMA reduce) and stored with TMA.
 // Per SM and chunk this moves 32 KB through TMA and shared memory (a single
 // CTA with a 128 x 256 tile needs 48 KB) for the same tensor-core work.
 // Every wait is bounded: a stalled pipeline records FP8BQ_ERR_TIMEOUT in the
@@ -89,6 +90,8 @@ struct GemmParams {
     int I, J, KC;         // output rows, output columns, reduction chunks
     int tiles_n;          // ceil(J / kBN)
     int num_tiles;        // ceil(I / kPairM) * tiles_n
+    int out_f32;          // D is FP32 (else BF16)
+    int accumulate;       // FP32 D: add into it (TMA reduce-add) instead of overwriting
     uint64_t timeout_ns;
 };
 
@@ -402,34 +405,61 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 if (buf == 0) tph ^= 1;
             }
             if (!ok) break;
-            // Epilogue: round to BF16 into this warp's swizzled staging boxes,
-            // then one lane issues the TMA stores (asynchronous: they drain
-            // while the next tile's chunks are promoted).
+            // Epilogue: round to BF16 (or keep FP32) into this warp's swizzled
+            // staging box, then one lane issues the TMA store or reduce-add
+            // (asynchronous: the last one drains while the next tile's chunks
+            // are promoted).
             uint8_t* stg = smEpi + pw * kEpiWarpBytes;
             const int y0 = r0 + quarter * 32;
             const bool store = hv && rv;
+            if (!p.out_f32) {
+                // BF16: four boxes of 32 rows x 32 columns
 #pragma unroll
-            for (int bx = 0; bx < 4; ++bx) {
-                uint8_t* box = stg;
-                // the previous box's store has finished reading the buffer
-                if (lane == 0) bulk_wait_group_read<0>();
-                __syncwarp();
+                for (int bx = 0; bx < 4; ++bx) {
+                    // the previous box's store has finished reading the buffer
+                    if (lane == 0) bulk_wait_group_read<0>();
+                    __syncwarp();
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float* a = acc + bx * 32 + j * 8;
-                    uint4 o;
-                    o.x = pack_bf16x2(a[0], a[1]);
-                    o.y = pack_bf16x2(a[2], a[3]);
-                    o.z = pack_bf16x2(a[4], a[5]);
-                    o.w = pack_bf16x2(a[6], a[7]);
-                    // 64-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ ((r >> 1) & 3)
-                    *reinterpret_cast<uint4*>(box + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) = o;
+                    for (int j = 0; j < 4; ++j) {
+                        const float* a = acc + bx * 32 + j * 8;
+                        uint4 o;
+                        o.x = pack_bf16x2(a[0], a[1]);
+                        o.y = pack_bf16x2(a[2], a[3]);
+                        o.z = pack_bf16x2(a[4], a[5]);
+                        o.w = pack_bf16x2(a[6], a[7]);
+                        // 64-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ ((r >> 1) & 3)
+                        *reinterpret_cast<uint4*>(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) = o;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (store) tma_store_2d(&tmD, smem_addr(stg), jh + bx * 32, y0);
+                        bulk_commit_group();
+                    }
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    if (store) tma_store_2d(&tmD, smem_addr(box), jh + bx * 32, y0);
-                    bulk_commit_group();
+            } else {
+                // FP32: eight boxes of 32 rows x 16 columns, stored or added
+#pragma unroll
+                for (int bx = 0; bx < 8; ++bx) {
+                    if (lane == 0) bulk_wait_group_read<0>();
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float* a = acc + bx * 16 + j * 4;
+                        *reinterpret_cast<float4*>(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
+                            make_float4(a[0], a[1], a[2], a[3]);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (store) {
+                            if (p.accumulate)
+                                tma_reduce_add_2d(&tmD, smem_addr(stg), jh + bx * 16, y0);
+                            else
+                                tma_store_2d(&tmD, smem_addr(stg), jh + bx * 16, y0);
+                        }
+                        bulk_commit_group();
+                    }
                 }
             }
         }

@@ -27,7 +27,7 @@ BF16, F32 = 0, 1
 C_FUNCTIONS = (
     "fp8bq_quantize_rowwise", "fp8bq_quantize_colwise", "fp8bq_quantize_rowcol",
     "fp8bq_quantize_weight_block", "fp8bq_gemm_fprop", "fp8bq_gemm_dgrad", "fp8bq_gemm_wgrad",
-    "fp8bq_check", "fp8bq_status_string", "fp8bq_selftest_wait_timeout",
+    "fp8bq_gemm_wgrad_f32", "fp8bq_check", "fp8bq_status_string", "fp8bq_selftest_wait_timeout",
 )
 
 
@@ -46,6 +46,7 @@ def _load():
         "fp8bq_gemm_fprop": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
         "fp8bq_gemm_dgrad": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
         "fp8bq_gemm_wgrad": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
+        "fp8bq_gemm_wgrad_f32": [vp, vp, vp, vp, vp, i64, i64, i64, i32, vp],
         "fp8bq_check": [vp],
         "fp8bq_selftest_wait_timeout": [i64, vp],
     }
@@ -209,6 +210,20 @@ def fp8bq_gemm_wgrad(dyqT, sdyT, xqT, sxT, dw) -> None:
                "fp8bq_gemm_wgrad")
 
 
+def fp8bq_gemm_wgrad_f32(dyqT, sdyT, xqT, sxT, dw, accumulate: bool = False) -> None:
+    """dW [N, K] float32 = dY^T X over tokens (accumulate: dW += dY^T X), operands as fp8bq_gemm_wgrad."""
+    N, M = dyqT.shape
+    K = xqT.shape[0]
+    _need(dyqT, torch.uint8, (N, M), "dyqT")
+    _need(sdyT, torch.float32, (M // 128, N), "sdyT")
+    _need(xqT, torch.uint8, (K, M), "xqT")
+    _need(sxT, torch.float32, (M // 128, K), "sxT")
+    _need(dw, torch.float32, (N, K), "dw")
+    with torch.cuda.device(dw.device):
+        _raise(lib.fp8bq_gemm_wgrad_f32(_ptr(dyqT), _ptr(sdyT), _ptr(xqT), _ptr(sxT), _ptr(dw), M, N, K,
+                                        1 if accumulate else 0, _stream(dw)), "fp8bq_gemm_wgrad_f32")
+
+
 def fp8bq_check(device=None) -> None:
     """Synchronize the current stream and raise if a kernel reported a device-side timeout."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
@@ -282,6 +297,12 @@ def gemm_dgrad(dyq, sdy, wqT, sw) -> torch.Tensor:
 def gemm_wgrad(dyqT, sdyT, xqT, sxT) -> torch.Tensor:
     dw = torch.empty((dyqT.shape[0], xqT.shape[0]), dtype=torch.bfloat16, device=dyqT.device)
     fp8bq_gemm_wgrad(dyqT, sdyT, xqT, sxT, dw)
+    return dw
+
+
+def gemm_wgrad_f32(dyqT, sdyT, xqT, sxT) -> torch.Tensor:
+    dw = torch.empty((dyqT.shape[0], xqT.shape[0]), dtype=torch.float32, device=dyqT.device)
+    fp8bq_gemm_wgrad_f32(dyqT, sdyT, xqT, sxT, dw)
     return dw
 
 

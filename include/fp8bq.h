@@ -152,6 +152,21 @@ int fp8bq_gemm_wgrad(const uint8_t* dyqT, const float* sdyT, const uint8_t* xqT,
                      uint16_t* dw, int64_t M, int64_t N, int64_t K, fp8bq_stream_t stream);
 
 /*
+ * Wgrad with an FP32 output, for keeping weight gradients in FP32 across
+ * micro-batches and data-parallel ranks (the Puro-2B report keeps training
+ * state in FP32, section 2 "FP8").  Same operands and product as
+ * fp8bq_gemm_wgrad; the result is not rounded to BF16.
+ *   dw          [N][K] FP32, dense
+ *   accumulate  0: dw = dY^T X;  1: dw += dY^T X (each element is added once,
+ *               in FP32, in L2; dw must hold the running sum on entry)
+ * Requires M, N, K % 128 == 0 and accumulate in {0, 1} (else FP8BQ_ERR_SHAPE).
+ * The adds of accumulate = 1 are atomic per element: calls that overlap in
+ * time on the same dw still sum correctly, in an unspecified order.
+ */
+int fp8bq_gemm_wgrad_f32(const uint8_t* dyqT, const float* sdyT, const uint8_t* xqT, const float* sxT,
+                         float* dw, int64_t M, int64_t N, int64_t K, int accumulate, fp8bq_stream_t stream);
+
+/*
  * Synchronize `stream`, then read and clear the current device's status word.
  * Returns FP8BQ_OK, FP8BQ_ERR_TIMEOUT if a kernel launched since the last
  * check gave up on a pipeline wait (its outputs are then undefined), or

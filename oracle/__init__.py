@@ -30,6 +30,9 @@ Functions and what pins them (tests/test_oracle_*.py):
                                 integer cases, single-chunk scale selection
   gemm_tolerance                the acceptance bound: |C - C_exact| <=
                                 2e-3 * sum_k |a_k b_k| + 1 BF16 ulp
+  f32_ulp / gemm_tolerance_f32  the same bound for FP32 outputs (one FP32 ulp;
+                                one more for an add into an FP32 array),
+                                pinned against numpy's spacing()
 """
 from __future__ import annotations
 
@@ -288,6 +291,40 @@ def gemm_tolerance(exact, abs_sum) -> np.ndarray:
     """Per-element acceptance bound: 2e-3 * sum_k |a_k b_k| + ulp_bf16(bf16(exact))."""
     ref = bf16_bits_to_f64(bf16_from_double(exact))
     return 2e-3 * np.asarray(abs_sum, dtype=np.float64) + bf16_ulp(ref)
+
+
+def f32_ulp(ref) -> np.ndarray:
+    """One binary32 unit in the last place at |ref|: 2^(max(floor(log2|ref|), -126) - 23); 2^-149 at 0."""
+    ref = np.abs(np.asarray(ref, dtype=np.float64))
+    _, ex = np.frexp(ref)
+    e = np.maximum(ex - 1, -126)
+    return np.where(ref == 0.0, np.ldexp(1.0, -149), np.ldexp(1.0, e - 23))
+
+
+def gemm_tolerance_f32(exact, abs_sum, base=None) -> np.ndarray:
+    """Acceptance bound for an FP32 GEMM output (the Wgrad variant that keeps
+    weight gradients in FP32): the same 2e-3 * sum_k |a_k b_k| term, with one
+    FP32 ulp of the exact value in place of the BF16 ulp, plus one FP32 ulp of
+    the final sum when the product is added into an FP32 array `base`."""
+    exact = np.asarray(exact, dtype=np.float64)
+    tol = 2e-3 * np.asarray(abs_sum, dtype=np.float64) + f32_ulp(exact)
+    if base is not None:
+        tol = tol + f32_ulp(np.asarray(base, dtype=np.float64) + exact)
+    return tol
+
+
+def gemm_check_f32(got_f32, exact, abs_sum, base=None):
+    """Compare FP32 outputs with the binary64 oracle (optionally base + product).
+    Returns (ok: bool, worst_ratio: float, err array)."""
+    got = np.asarray(got_f32, dtype=np.float32).astype(np.float64)
+    want = np.asarray(exact, dtype=np.float64)
+    if base is not None:
+        want = np.asarray(base, dtype=np.float32).astype(np.float64) + want
+    err = np.abs(got - want)
+    tol = gemm_tolerance_f32(exact, abs_sum, None if base is None else np.asarray(base, dtype=np.float32))
+    ratio = err / tol
+    worst = float(np.max(ratio)) if ratio.size else 0.0
+    return bool(np.all(err <= tol) and np.all(np.isfinite(got))), worst, err
 
 
 def gemm_check(got_bf16_bits, exact, abs_sum):

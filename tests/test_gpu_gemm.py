@@ -178,3 +178,86 @@ def test_full_size_up_proj_backward_sampled(fb):
     sdyT, sxT = random_scales(rng, (M // 128, N)), random_scales(rng, (M // 128, K))
     dw = _wgrad(fb, dyqT, sdyT, xqT, sxT)
     check_gemm_tiles(dw, oracle.gemm_wgrad, (dyqT, sdyT, xqT, sxT), sample_tiles(rng, N, K, 4), what="wgrad full")
+
+
+# ---------------------------------------------------------------------------
+# Wgrad with an FP32 output (overwrite or accumulate into)
+# ---------------------------------------------------------------------------
+
+def _check_f32_tiles(got_dev, oracle_fn, args, picks, base=None, tile=128, what=""):
+    got = got_dev.cpu().numpy()
+    for (bi, bj) in picks:
+        rows = np.arange(bi * tile, (bi + 1) * tile)
+        cols = np.arange(bj * tile, (bj + 1) * tile)
+        exact, absd = oracle_fn(*args, rows=rows, cols=cols)
+        b = None if base is None else base[np.ix_(rows, cols)]
+        ok, ratio, err = oracle.gemm_check_f32(got[np.ix_(rows, cols)], exact, absd, base=b)
+        assert ok, f"{what} tile ({bi},{bj}): worst error/tolerance {ratio:.3g}"
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (640, 384, 256), (256, 256, 640)])
+def test_wgrad_f32_random_codes(fb, M, N, K):
+    rng = np.random.default_rng(13 * M + N + K)
+    dyqT, xqT = random_codes(rng, (N, M)), random_codes(rng, (K, M))
+    sdyT, sxT = random_scales(rng, (M // 128, N)), random_scales(rng, (M // 128, K))
+    dev = [to_dev(a) for a in (dyqT, sdyT, xqT, sxT)]
+    dw = fb.gemm_wgrad_f32(*dev)
+    fb.check()
+    assert dw.dtype == torch.float32 and dw.shape == (N, K)
+    _check_f32_tiles(dw, oracle.gemm_wgrad, (dyqT, sdyT, xqT, sxT), _all_tiles(N, K), what=f"wgrad f32 {M}x{N}x{K}")
+    # the BF16 kernel rounds the same FP32 accumulators: identical after RNE
+    dw16 = fb.gemm_wgrad(*dev)
+    fb.check()
+    assert torch.equal(dw.to(torch.bfloat16), dw16)
+
+
+def test_wgrad_f32_accumulates_into_the_output(fb):
+    rng = np.random.default_rng(41)
+    M, N, K = 384, 256, 384
+    dyqT, xqT = random_codes(rng, (N, M)), random_codes(rng, (K, M))
+    sdyT, sxT = random_scales(rng, (M // 128, N)), random_scales(rng, (M // 128, K))
+    base = (rng.normal(0, 50, (N, K))).astype(np.float32)
+    dw = to_dev(base)
+    fb.fp8bq_gemm_wgrad_f32(to_dev(dyqT), to_dev(sdyT), to_dev(xqT), to_dev(sxT), dw, accumulate=True)
+    fb.check()
+    _check_f32_tiles(dw, oracle.gemm_wgrad, (dyqT, sdyT, xqT, sxT), _all_tiles(N, K), base=base,
+                     what="wgrad f32 accumulate")
+
+
+def test_wgrad_f32_token_shards_sum_to_the_full_product(fb):
+    """Accumulating the Wgrad of consecutive token shards into one FP32 array
+    gives the Wgrad of all tokens (the data-parallel / micro-batch use)."""
+    rng = np.random.default_rng(42)
+    M, N, K = 768, 256, 384
+    dyqT, xqT = random_codes(rng, (N, M)), random_codes(rng, (K, M))
+    sdyT, sxT = random_scales(rng, (M // 128, N)), random_scales(rng, (M // 128, K))
+    dw = torch.zeros((N, K), dtype=torch.float32, device="cuda")
+    for m0, m1 in ((0, 256), (256, 640), (640, 768)):
+        fb.fp8bq_gemm_wgrad_f32(to_dev(np.ascontiguousarray(dyqT[:, m0:m1])), to_dev(sdyT[m0 // 128:m1 // 128]),
+                                to_dev(np.ascontiguousarray(xqT[:, m0:m1])), to_dev(sxT[m0 // 128:m1 // 128]), dw,
+                                accumulate=True)
+    fb.check()
+    exact, absd = oracle.gemm_wgrad(dyqT, sdyT, xqT, sxT)
+    ok, ratio, _ = oracle.gemm_check_f32(dw.cpu().numpy(), exact, absd)
+    assert ok, ratio
+
+
+def test_wgrad_f32_exact_integer_case_is_bit_exact(fb):
+    rng = np.random.default_rng(43)
+    M, N, K = 512, 384, 256
+    dyqT, _ = _integer_operands(rng, (N, M))
+    xqT, _ = _integer_operands(rng, (K, M))
+    sdyT = np.exp2(rng.integers(-2, 3, size=(M // 128, N))).astype(np.float32)
+    sxT = np.exp2(rng.integers(-2, 3, size=(M // 128, K))).astype(np.float32)
+    dw = fb.gemm_wgrad_f32(to_dev(dyqT), to_dev(sdyT), to_dev(xqT), to_dev(sxT))
+    fb.check()
+    exact, _ = oracle.gemm_wgrad(dyqT, sdyT, xqT, sxT)
+    assert np.array_equal(dw.cpu().numpy(), exact.astype(np.float32))
+    # empty reduction: overwrite writes zeros, accumulate leaves the array alone
+    z = torch.full((N, K), 7.0, dtype=torch.float32, device="cuda")
+    e8, e32 = torch.empty((N, 0), dtype=torch.uint8, device="cuda"), torch.empty((0, N), device="cuda")
+    k8, k32 = torch.empty((K, 0), dtype=torch.uint8, device="cuda"), torch.empty((0, K), device="cuda")
+    fb.fp8bq_gemm_wgrad_f32(e8, e32, k8, k32, z, accumulate=True)
+    assert torch.all(z == 7.0)
+    fb.fp8bq_gemm_wgrad_f32(e8, e32, k8, k32, z, accumulate=False)
+    assert torch.all(z == 0.0)

@@ -243,3 +243,32 @@ def test_bf16_ulp_and_tolerance():
     assert ok and worst == 1.0
     ok, _, _ = oracle.gemm_check(oracle.bf16_from_double(np.array([1.0 + 2 ** -6])), np.array([1.0]), np.array([0.0]))
     assert not ok
+
+
+def test_f32_ulp_matches_numpy_spacing():
+    """f32_ulp against numpy's nextafter-based spacing (upward gap) on normal,
+    subnormal and power-of-two magnitudes."""
+    rng = np.random.default_rng(31)
+    vals = np.concatenate([rng.uniform(-1e6, 1e6, 1000), np.ldexp(1.0, np.arange(-149, 120)),
+                           rng.uniform(0, 1, 100) * 2.0 ** -130]).astype(np.float32)
+    want = np.spacing(np.abs(vals)).astype(np.float64)
+    got = oracle.f32_ulp(vals.astype(np.float64))
+    assert np.array_equal(got, want)
+    assert oracle.f32_ulp(0.0) == 2.0 ** -149
+
+
+def test_f32_tolerance_accepts_rounding_and_rejects_one_extra_ulp_of_s():
+    """An FP32 output that is the correctly rounded exact value passes; the bound
+    grows by one FP32 ulp when the product is added into a base array."""
+    rng = np.random.default_rng(32)
+    exact = rng.normal(0, 3, 1000)
+    absd = np.abs(exact) * 1.5
+    ok, _, _ = oracle.gemm_check_f32(exact.astype(np.float32), exact, absd)
+    assert ok
+    bad = exact + 2e-3 * absd + 2 * oracle.f32_ulp(exact)
+    ok, _, _ = oracle.gemm_check_f32(bad, exact, absd)
+    assert not ok
+    base = rng.normal(0, 100, 1000).astype(np.float32)
+    summed = (base.astype(np.float64) + exact).astype(np.float32)
+    ok, _, _ = oracle.gemm_check_f32(summed, exact, absd, base=base)
+    assert ok
