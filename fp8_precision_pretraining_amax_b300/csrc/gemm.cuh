@@ -20,10 +20,10 @@
 //               6-stage shared-memory ring (128-byte swizzle), completion
 //               bytes counted on the even CTA's full barrier, which expects
 //               both CTAs' bytes.
-//   warp 2      scale producer (both CTAs): cp.async copies of each chunk's
-//               scales (this CTA's 128 row scales and the tile's column
-//               scales) into a 6-slot ring, so no promotion warp ever waits
-//               on a global-memory load.
+//   warp 2      scale producer (both CTAs): bulk and cp.async copies of each
+//               chunk's scales (this CTA's 128 row scales and the tile's
+//               column scales) into a 6-slot ring, so no promotion warp ever
+//               waits on a global-memory load.
 //   warp 1      allocates the pair's TMEM (both CTAs); in the even CTA one
 //               thread issues four tcgen05.mma.cta_group::2.kind::f8f6f4
 //               (256x256x32) per chunk into one of two TMEM partial buffers
@@ -108,7 +108,7 @@ struct alignas(16) GemmCtl {
     uint64_t empty[kStages];   // both CTAs: the pair MMA has read the stage (signalled by promotion warp 0)
     uint64_t tfull[2];         // both CTAs: the chunk partial is in TMEM
     uint64_t tempty[2];        // even CTA: both CTAs' promotion warps read it
-    uint64_t sfull[kScaleSlots];   // the slot's scale copies landed (32 producer lanes)
+    uint64_t sfull[kScaleSlots];   // the slot's scale copies landed
     uint64_t sempty[kScaleSlots];  // the promotion warps are done with the slot (8 warps)
     uint64_t drain;
     uint32_t tmem_base;
@@ -128,6 +128,16 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
                                           uint64_t limit_ns) {
     int ok = 0;
     if ((threadIdx.x & 31) == 0) ok = bounded_wait(bar, parity, abort_flag, limit_ns) ? 1 : 0;
+    return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+}
+
+// warp_wait for the scale producer, which runs far ahead: lane 0 backs off
+// between polls so the promotion warps of its SM sub-partition keep their
+// issue slots.
+__device__ __forceinline__ bool warp_wait_backoff(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                  uint64_t limit_ns) {
+    int ok = 0;
+    if ((threadIdx.x & 31) == 0) ok = bounded_wait_backoff(bar, parity, abort_flag, limit_ns, 128) ? 1 : 0;
     return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
 }
 
@@ -191,7 +201,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(&ctl->tempty[b], 2 * kPromoWarps);
         }
         for (int q = 0; q < kScaleSlots; ++q) {
-            mbar_init(&ctl->sfull[q], 32);
+            // one expect_tx arrival for the bulk copies, plus the two cp.async
+            // arrivals of the weight-block scales in Fprop/Dgrad
+            mbar_init(&ctl->sfull[q], MODE == kModeWgrad ? 1 : 3);
             mbar_init(&ctl->sempty[q], kPromoWarps);
         }
         mbar_init(&ctl->drain, 1);
@@ -249,36 +261,36 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else if (warp == 2) {
         // --------------------------------------------------- scale producer
         // Copies each chunk's scales into the next ring slot: this CTA's 128
-        // row scales, and the tile's column scales (Wgrad: 256 values;
-        // Fprop/Dgrad: the weight-block scale of each 128-column half).
-        // Rows and columns past the problem are skipped.
+        // row scales and Wgrad's column scales with bulk copies (one lane,
+        // completion in bytes), Fprop/Dgrad's weight-block scale of each
+        // 128-column half with two 4-byte cp.async.  Rows and columns past
+        // the problem are skipped.
         uint32_t q = 0, qph = 0;
         bool ok = true;
         for (int tile = first_tile; tile < p.num_tiles && ok; tile += tile_step) {
             const int tm = tile / p.tiles_n, tn = tile - tm * p.tiles_n;
             const int r0 = tm * kPairM + static_cast<int>(rank) * kBM;
             const int j0 = tn * kBN;
+            const uint32_t a_bytes = r0 < p.I ? 128u * 4u : 0u;
+            const uint32_t b_bytes = MODE == kModeWgrad ? static_cast<uint32_t>(min(p.J - j0, kBN)) * 4u : 0u;
             for (int c = 0; c < p.KC; ++c) {
-                if (!warp_wait(&ctl->sempty[q], qph ^ 1, abort_flag, lim)) { ok = false; break; }
+                if (!warp_wait_backoff(&ctl->sempty[q], qph ^ 1, abort_flag, lim)) { ok = false; break; }
                 ScaleSlot& sl = ctl->scl[q];
-                if (r0 < p.I)
-                    cp_async_16g(smem_addr(&sl.a[4 * lane]), p.sA + static_cast<int64_t>(c) * p.I + r0 + 4 * lane);
-                if (MODE == kModeWgrad) {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int j = j0 + h * 128 + 4 * lane;
-                        if (j < p.J)
-                            cp_async_16g(smem_addr(&sl.b[h * 128 + 4 * lane]), p.sB + static_cast<int64_t>(c) * p.J + j);
-                    }
-                } else if (lane < 2) {
+                if (lane == 0) {
+                    const uint32_t bar = smem_addr(&ctl->sfull[q]);
+                    mbar_arrive_expect_tx(&ctl->sfull[q], a_bytes + b_bytes);
+                    if (a_bytes) bulk_load(smem_addr(sl.a), p.sA + static_cast<int64_t>(c) * p.I + r0, a_bytes, bar);
+                    if (b_bytes) bulk_load(smem_addr(sl.b), p.sB + static_cast<int64_t>(c) * p.J + j0, b_bytes, bar);
+                }
+                if (MODE != kModeWgrad && lane < 2) {
                     const int jb = (j0 >> 7) + lane;  // 128-column block of the weight
                     if (jb * 128 < p.J) {
                         const float* src = MODE == kModeFprop ? p.sB + static_cast<int64_t>(jb) * p.KC + c
                                                               : p.sB + static_cast<int64_t>(c) * (p.J >> 7) + jb;
                         cp_async_4(smem_addr(&sl.b[lane]), src);
                     }
+                    cp_async_arrive(&ctl->sfull[q]);
                 }
-                cp_async_arrive(&ctl->sfull[q]);
                 if (++q == kScaleSlots) { q = 0; qph ^= 1; }
             }
         }

@@ -98,6 +98,22 @@ __device__ __forceinline__ bool bounded_spin(uint64_t* bar, uint32_t parity, vol
     }
 }
 
+// bounded_wait for a thread that is usually far ahead of its consumers (the
+// copy producers): between polls it sleeps `sleep_ns`, so the warps it shares
+// an SM sub-partition with keep its issue slots.
+__device__ __forceinline__ bool bounded_wait_backoff(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                     uint64_t limit_ns, uint32_t sleep_ns) {
+    const uint32_t a = smem_addr(bar);
+    if (mbar_try_wait(a, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        __nanosleep(sleep_ns);
+        if (mbar_try_wait(a, parity)) return true;
+        if (abort_flag != nullptr && *abort_flag) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
 // --------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
@@ -112,6 +128,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         "[%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
         : "memory");
+}
+
+// Contiguous global -> shared bulk copy of `bytes` (a multiple of 16, both
+// addresses 16-byte aligned), completion counted on `bar` (tx bytes).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
 }
 
 // 2-D tiled store shared -> global (bulk-group completion).
