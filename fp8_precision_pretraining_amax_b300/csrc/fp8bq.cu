@@ -232,8 +232,8 @@ int fp8bq_quantize_rowwise(const void* x, int dtype, int64_t R, int64_t C, int64
     int st = probe_device(&dev);
     if (st != FP8BQ_OK) return st;
     const int64_t tiles = R * (C / 128);
-    const int64_t blocks = (tiles + 31) / 32;  // 8 warps x 4 tiles
-    if (blocks >= (int64_t(1) << 31)) return FP8BQ_ERR_SHAPE;
+    if (tiles >= (int64_t(1) << 31)) return FP8BQ_ERR_SHAPE;  // the kernel indexes tiles in 32 bits
+    const int64_t blocks = (tiles + 31) / 32;                    // 8 warps x 4 tiles
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     if (dtype == FP8BQ_BF16)
         fp8bq::quantize_rowwise_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, cs>>>(x, R, C, ldx, q, s);

@@ -41,21 +41,30 @@ __device__ __forceinline__ float tile_scale(float amax) {
 // exhaustively over every pair of BF16 values (x, amax), |x| <= amax.
 constexpr float kRecipMinAmax = 0x1p-80f;
 
-// Per-tile divisor: the scale, its correctly rounded reciprocal, and whether
-// the one-step reciprocal quotient applies.
+// Per-tile divisor: the scale, its negation and its correctly rounded
+// reciprocal.  r == 0 marks a tile that needs IEEE division (amax < 2^-80);
+// this lets the divisor travel through shared memory as two floats.
 struct TileDiv {
     float s, ns, r;
-    bool fast;
 };
 
 __device__ __forceinline__ TileDiv tile_div(float amax) {
     TileDiv d;
     d.s = tile_scale(amax);
     d.ns = -d.s;
-    d.r = __frcp_rn(d.s);
-    d.fast = amax >= kRecipMinAmax;
+    d.r = amax >= kRecipMinAmax ? __frcp_rn(d.s) : 0.0f;
     return d;
 }
+
+__device__ __forceinline__ TileDiv tile_div_from(float s, float r) {
+    TileDiv d;
+    d.s = s;
+    d.ns = -s;
+    d.r = r;
+    return d;
+}
+
+__device__ __forceinline__ bool tile_fast(const TileDiv& d) { return d.r != 0.0f; }
 
 // Sign of x copied onto q: x / s carries the sign of x (s > 0), which the
 // correction step below loses for x = -0 only.
@@ -68,9 +77,11 @@ __device__ __forceinline__ float with_sign_of(float q, float x) {
 // System/6000 processor", IBM J. Res. Dev. 34(1), 1990): with r = RN(1/s),
 // q0 = RN(x r) lies within one ulp of x / s, the residual x - q0 s is exact
 // under FMA, and q0 + r (x - q0 s) rounded once is RN(x / s).  Packed f32x2
-// arithmetic, two quotients per instruction.
+// arithmetic, two quotients per instruction.  The slow path (tiny tiles) is
+// IEEE division.  Callers choose the path once per tile.
+template <bool kFast>
 __device__ __forceinline__ float2 quot2(float a, float b, const TileDiv& d) {
-    if (!d.fast) return make_float2(__fdiv_rn(a, d.s), __fdiv_rn(b, d.s));
+    if (!kFast) return make_float2(__fdiv_rn(a, d.s), __fdiv_rn(b, d.s));
     float q0a, q0b;
     fmul2(q0a, q0b, a, b, d.r, d.r);
     float ea = a, eb = b;
@@ -80,14 +91,34 @@ __device__ __forceinline__ float2 quot2(float a, float b, const TileDiv& d) {
 }
 
 // Two values -> two E4M3 codes packed low byte first (element a first).
+template <bool kFast>
 __device__ __forceinline__ uint32_t e4m3x2(float a, float b, const TileDiv& d) {
-    return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(quot2(a, b, d), __NV_SATFINITE, __NV_E4M3));
+    return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(quot2<kFast>(a, b, d), __NV_SATFINITE, __NV_E4M3));
 }
 
 // Four values -> four codes in one 32-bit word (memory order).
+template <bool kFast>
 __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float e, const TileDiv& d) {
-    return e4m3x2(a, b, d) | (e4m3x2(c, e, d) << 16);
+    return e4m3x2<kFast>(a, b, d) | (e4m3x2<kFast>(c, e, d) << 16);
 }
+
+// Eight values -> eight codes (memory order), path chosen per tile.
+__device__ __forceinline__ uint2 e4m3x8(const float* v, const TileDiv& d) {
+    if (tile_fast(d))
+        return make_uint2(e4m3x4<true>(v[0], v[1], v[2], v[3], d), e4m3x4<true>(v[4], v[5], v[6], v[7], d));
+    return make_uint2(e4m3x4<false>(v[0], v[1], v[2], v[3], d), e4m3x4<false>(v[4], v[5], v[6], v[7], d));
+}
+
+// Lane-wise max of |a| and |b| for two packed BF16 pairs (sign bits cleared,
+// then one bf16x2 max).  Inputs are finite (NaN is outside the contract).
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a & 0x7FFF7FFFu), "r"(b & 0x7FFF7FFFu));
+    return d;
+}
+
+// max(|lo|, |hi|) of a packed pair whose sign bits are already clear, as FP32.
+__device__ __forceinline__ float bf16x2_max_halves(uint32_t m) { return fmaxf(bf16lo(m), bf16hi(m)); }
 
 __device__ __forceinline__ void unpack_bf16x8(const uint4& w, float (&v)[8]) {
     v[0] = bf16lo(w.x); v[1] = bf16hi(w.x);
@@ -115,41 +146,79 @@ __device__ __forceinline__ void cp_async_wait_all() {
 
 // ------------------------------------------------------------------ row-wise
 //
-// One 1x128 tile per group of 8 lanes (4 tiles per warp).  Lane j of a group
-// owns elements [8j, 8j+8) and [64+8j, 64+8j+8) of its tile (16 values), so
-// each warp-wide 16-byte load reads 4 fully used 128-byte segments.  Tiles are
-// numbered row-major (tile = r * C/128 + t) so consecutive warps stream
-// consecutive memory.
+// Helpers for a 1x128 row tile held by 4 lanes (32 values each, lane j owning
+// the 16-byte chunks j, j+4, j+8, j+12), used by the slab kernel's row view.
 
+// amax of a tile spread over 4 lanes (lanes 4t..4t+3 of the warp).
+template <bool kF32>
+__device__ __forceinline__ float quarter_amax(const float (&v)[32], uint32_t pm) {
+    float a = 0.0f;
+    if (!kF32) {
+        a = bf16x2_max_halves(pm);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) a = fmaxf(a, fabsf(v[i]));
+    }
+    a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+    return fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+}
+
+// Writes the lane's 32 codes of a row tile to `dst` (its 128-byte row).
+// Register group k holds input chunk j + 4 (k ^ flip) (flip: 0 or 1 for BF16,
+// whose groups are 8 values; FP32 groups are 4 values and use flip 0).
+template <bool kF32>
+__device__ __forceinline__ void store_row_quarter(uint8_t* dst, int j, const float (&v)[32], const TileDiv& d,
+                                                  int flip = 0) {
+    if (!kF32) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            *reinterpret_cast<uint2*>(dst + 8 * (j + 4 * (k ^ flip))) = e4m3x8(v + 8 * k, d);
+    } else {
+        // FP32 chunks hold 4 values: lane j owns chunks j + 4k, k = 0..7
+#pragma unroll
+        for (int k = 0; k < 8; k += 2) {
+            const uint2 c = e4m3x8(v + 4 * k, d);  // chunks j+4k and j+4k+4
+            *reinterpret_cast<uint32_t*>(dst + 4 * (j + 4 * k)) = c.x;
+            *reinterpret_cast<uint32_t*>(dst + 4 * (j + 4 * k + 4)) = c.y;
+        }
+    }
+}
+
+// Streaming kernel: one 1x128 tile per group of 8 lanes (4 tiles per warp),
+// lane j owning elements [8j, 8j+8) and [64+8j, 64+8j+8) (BF16) or
+// [4j + 32p, 4j + 32p + 4), p = 0..3 (FP32), so each warp-wide 16-byte load
+// reads whole 128-byte lines.
 template <bool kF32>
 __global__ void __launch_bounds__(256) quantize_rowwise_kernel(const void* __restrict__ x, int64_t R, int64_t C,
                                                                int64_t ldx, uint8_t* __restrict__ q,
                                                                float* __restrict__ s) {
     const int lane = threadIdx.x & 31;
     const int j = lane & 7;
-    const int64_t T = C >> 7;
-    const int64_t ntiles = R * T;
-    const int64_t tile = ((static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5)) << 2) + (lane >> 3);
+    const uint32_t T = static_cast<uint32_t>(C >> 7);
+    const uint32_t ntiles = static_cast<uint32_t>(R) * T;  // < 2^31 (checked on the host)
+    const uint32_t tile = (blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 4u + (lane >> 3);
     const bool valid = tile < ntiles;
-    const int64_t r = valid ? tile / T : 0;
-    const int64_t t = valid ? tile - r * T : 0;
+    const uint32_t r = valid ? tile / T : 0;
+    const uint32_t t = valid ? tile - r * T : 0;
 
     float v[16];
+    float amax = 0.0f;
     if (!kF32) {
-        const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(x) + r * ldx + t * 128;
-        uint4 w0 = make_uint4(0, 0, 0, 0), w1 = make_uint4(0, 0, 0, 0);
+        const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(x) + static_cast<int64_t>(r) * ldx + t * 128;
+        uint4 wa = make_uint4(0, 0, 0, 0), wb = make_uint4(0, 0, 0, 0);
         if (valid) {
-            w0 = ldg_nc_v4(src + 8 * j);
-            w1 = ldg_nc_v4(src + 64 + 8 * j);
+            wa = ldg_nc_v4(src + 8 * j);
+            wb = ldg_nc_v4(src + 64 + 8 * j);
         }
+        amax = bf16x2_max_halves(absmax_bf16x2(absmax_bf16x2(absmax_bf16x2(wa.x, wa.y), absmax_bf16x2(wa.z, wa.w)),
+                                               absmax_bf16x2(absmax_bf16x2(wb.x, wb.y), absmax_bf16x2(wb.z, wb.w))));
         float a[8], b[8];
-        unpack_bf16x8(w0, a);
-        unpack_bf16x8(w1, b);
+        unpack_bf16x8(wa, a);
+        unpack_bf16x8(wb, b);
 #pragma unroll
         for (int i = 0; i < 8; ++i) { v[i] = a[i]; v[8 + i] = b[i]; }
     } else {
-        // lane j owns elements [4j + 32p, 4j + 32p + 4), p = 0..3
-        const float* src = static_cast<const float*>(x) + r * ldx + t * 128;
+        const float* src = static_cast<const float*>(x) + static_cast<int64_t>(r) * ldx + t * 128;
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
             uint4 w = make_uint4(0, 0, 0, 0);
@@ -159,30 +228,27 @@ __global__ void __launch_bounds__(256) quantize_rowwise_kernel(const void* __res
             v[4 * p + 2] = __uint_as_float(w.z);
             v[4 * p + 3] = __uint_as_float(w.w);
         }
-    }
-
-    float amax = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    }
     amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
     amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
     const TileDiv d = tile_div(amax);
 
     if (!valid) return;
-    uint8_t* dst = q + r * C + t * 128;
+    uint8_t* dst = q + static_cast<int64_t>(r) * C + t * 128;
     if (!kF32) {
-        *reinterpret_cast<uint2*>(dst + 8 * j) =
-            make_uint2(e4m3x4(v[0], v[1], v[2], v[3], d), e4m3x4(v[4], v[5], v[6], v[7], d));
-        *reinterpret_cast<uint2*>(dst + 64 + 8 * j) =
-            make_uint2(e4m3x4(v[8], v[9], v[10], v[11], d), e4m3x4(v[12], v[13], v[14], v[15], d));
+        *reinterpret_cast<uint2*>(dst + 8 * j) = e4m3x8(v, d);
+        *reinterpret_cast<uint2*>(dst + 64 + 8 * j) = e4m3x8(v + 8, d);
     } else {
-#pragma unroll
-        for (int p = 0; p < 4; ++p)
-            *reinterpret_cast<uint32_t*>(dst + 32 * p + 4 * j) =
-                e4m3x4(v[4 * p], v[4 * p + 1], v[4 * p + 2], v[4 * p + 3], d);
+        const uint2 c0 = e4m3x8(v, d), c1 = e4m3x8(v + 8, d);
+        *reinterpret_cast<uint32_t*>(dst + 4 * j) = c0.x;
+        *reinterpret_cast<uint32_t*>(dst + 32 + 4 * j) = c0.y;
+        *reinterpret_cast<uint32_t*>(dst + 64 + 4 * j) = c1.x;
+        *reinterpret_cast<uint32_t*>(dst + 96 + 4 * j) = c1.y;
     }
-    if (j == 0) s[t * R + r] = d.s;
+    if (j == 0) s[static_cast<int64_t>(t) * R + r] = d.s;
 }
 
 // ------------------------------------------------------------- 128x128 slabs
@@ -190,15 +256,18 @@ __global__ void __launch_bounds__(256) quantize_rowwise_kernel(const void* __res
 // CTA = 256 threads, one slab of 128 rows x 128 columns (rows r0.., columns
 // c0..; all 128 rows exist, trailing columns past C read as zero and are not
 // written).  The slab is copied to shared memory with 16-byte cp.async
-// (row pitch 128 * element size), then read in two ways, both free of bank
-// conflicts because every warp access covers contiguous bytes of one row:
+// (row pitch 128 * element size), then read in two ways:
 //   column view  thread = (4-byte unit u of a row, group g of rows): BF16 has
 //                64 units (column pairs) x 4 groups of 32 rows, FP32 128
-//                units (columns) x 2 groups of 64 rows.  Per-column amax over
-//                the group, combined over groups in shared memory; codes of
-//                a column's rows are contiguous in the transposed output.
-//   row view     8 lanes per row, 16 values per lane (the row-wise kernel's
-//                mapping), 32 rows per pass, 4 passes.
+//                units (columns) x 2 groups of 64 rows.  A warp reads 128
+//                contiguous bytes of one row (no bank conflicts).  Partial
+//                column amaxes meet in shared memory; one thread per column
+//                forms its divisor, which every group then reads; codes of a
+//                column's rows are contiguous in the transposed output.
+//   row view     4 lanes per row, 32 values per lane (chunks j + 4k), 64 rows
+//                per pass, 2 passes; odd rows take their chunks in the order
+//                k ^ 1 so the two rows a quarter-warp reads hit different
+//                banks.
 // Modes:
 //   kTileCol     column-wise 128x1 tiles: qT [C][R], s_col [R/128][C]
 //   kTileDual    row-wise 1x128 and column-wise 128x1 tiles of the same
@@ -225,6 +294,7 @@ __global__ void __launch_bounds__(256) quantize_tile_kernel(const void* __restri
     constexpr int RPG = 128 / G;      // rows per group
     extern __shared__ __align__(16) uint8_t slab[];
     __shared__ float red[G][128];
+    __shared__ float cdiv[2][128];    // per column (or [.][0] for the block): s, r
     __shared__ float wred[8];
 
     const int tid = threadIdx.x;
@@ -246,33 +316,42 @@ __global__ void __launch_bounds__(256) quantize_tile_kernel(const void* __restri
     cp_async_wait_all();
     __syncthreads();
 
-    // ---- column view: amax of this thread's column(s) over its row group
+    // ---- column view: this thread's column(s) over its row group (BF16:
+    //      kept in registers for the code pass; FP32 re-reads shared memory)
     const int u = tid % UPR, g = tid / UPR;
     const uint8_t* colp = slab + g * RPG * RB + u * 4;
+    constexpr int NCW = kF32 ? 1 : RPG;
+    uint32_t cw[NCW];
+    auto colword = [&](int i) -> uint32_t {
+        return kF32 ? *reinterpret_cast<const uint32_t*>(colp + i * RB) : cw[kF32 ? 0 : i];
+    };
     float cmax[VEC];
+    if (!kF32) {
+        uint32_t m = 0;
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) cmax[e] = 0.0f;
-#pragma unroll 8
-    for (int i = 0; i < RPG; ++i) {
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(colp + i * RB);
-        if (!kF32) {
-            cmax[0] = fmaxf(cmax[0], fabsf(bf16lo(w)));
-            cmax[VEC - 1] = fmaxf(cmax[VEC - 1], fabsf(bf16hi(w)));
-        } else {
-            cmax[0] = fmaxf(cmax[0], fabsf(__uint_as_float(w)));
+        for (int i = 0; i < NCW; ++i) {
+            cw[i] = *reinterpret_cast<const uint32_t*>(colp + i * RB);
+            m = absmax_bf16x2(m, cw[i]);
         }
+        cmax[0] = bf16lo(m);
+        cmax[VEC - 1] = bf16hi(m);
+    } else {
+        cmax[0] = 0.0f;
+#pragma unroll 8
+        for (int i = 0; i < RPG; ++i) cmax[0] = fmaxf(cmax[0], fabsf(__uint_as_float(colword(i))));
     }
-    TileDiv cd[VEC];
     if (kMode != kTileWeight) {
 #pragma unroll
         for (int e = 0; e < VEC; ++e) red[g][u * VEC + e] = cmax[e];
         __syncthreads();
+        if (tid < 128) {  // one thread per column forms the divisor
+            float a = red[0][tid];
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-            float a = red[0][u * VEC + e];
-#pragma unroll
-            for (int gg = 1; gg < G; ++gg) a = fmaxf(a, red[gg][u * VEC + e]);
-            cd[e] = tile_div(a);
+            for (int gg = 1; gg < G; ++gg) a = fmaxf(a, red[gg][tid]);
+            const TileDiv d = tile_div(a);
+            cdiv[0][tid] = d.s;
+            cdiv[1][tid] = d.r;
+            if (c0 + tid < C) s_col[(r0 >> 7) * C + c0 + tid] = d.s;
         }
     } else {
         float a = cmax[0];
@@ -282,60 +361,71 @@ __global__ void __launch_bounds__(256) quantize_tile_kernel(const void* __restri
         for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, off));
         if ((tid & 31) == 0) wred[tid >> 5] = a;
         __syncthreads();
-        a = wred[0];
+        if (tid == 0) {
+            a = wred[0];
 #pragma unroll
-        for (int w = 1; w < 8; ++w) a = fmaxf(a, wred[w]);
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) cd[e] = tile_div(a);
-        if (tid == 0) s_row[(r0 >> 7) * (C >> 7) + (c0 >> 7)] = cd[0].s;
+            for (int w = 1; w < 8; ++w) a = fmaxf(a, wred[w]);
+            const TileDiv d = tile_div(a);
+            cdiv[0][0] = d.s;
+            cdiv[1][0] = d.r;
+            s_row[(r0 >> 7) * (C >> 7) + (c0 >> 7)] = d.s;
+        }
     }
+    __syncthreads();
 
     // ---- column view: codes, transposed (qT[c][r0 + g*RPG ...], 16 rows per store)
     if (kMode != kTileWeight || qT != nullptr) {
 #pragma unroll
         for (int e = 0; e < VEC; ++e) {
-            const int64_t c = c0 + u * VEC + e;
+            const int cc = u * VEC + e;
+            const int64_t c = c0 + cc;
             if (c < C) {
+                const int di = kMode == kTileWeight ? 0 : cc;
+                const TileDiv d = tile_div_from(cdiv[0][di], cdiv[1][di]);
                 uint8_t* dst = qT + c * R + r0 + g * RPG;
 #pragma unroll
                 for (int h = 0; h < RPG / 16; ++h) {
-                    uint32_t wv[4];
+                    float f[16];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        float f[4];
-#pragma unroll
-                        for (int m = 0; m < 4; ++m) {
-                            const uint32_t w =
-                                *reinterpret_cast<const uint32_t*>(colp + (h * 16 + k * 4 + m) * RB);
-                            f[m] = kF32 ? __uint_as_float(w) : (e == 0 ? bf16lo(w) : bf16hi(w));
-                        }
-                        wv[k] = e4m3x4(f[0], f[1], f[2], f[3], cd[e]);
+                    for (int m = 0; m < 16; ++m) {
+                        const uint32_t w = colword(h * 16 + m);
+                        f[m] = kF32 ? __uint_as_float(w) : (e == 0 ? bf16lo(w) : bf16hi(w));
                     }
-                    *reinterpret_cast<uint4*>(dst + h * 16) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                    const uint2 lo = e4m3x8(f, d), hi = e4m3x8(f + 8, d);
+                    *reinterpret_cast<uint4*>(dst + h * 16) = make_uint4(lo.x, lo.y, hi.x, hi.y);
                 }
-                if (kMode != kTileWeight && g == 0) s_col[(r0 >> 7) * C + c] = cd[e].s;
             }
         }
     }
 
     // ---- row view: row-wise tiles (dual) or the block's row-major codes (weight)
     if (kMode == kTileCol) return;
-    const int j = tid & 7;
+    const int j = tid & 3;
 #pragma unroll 1
-    for (int p = 0; p < 4; ++p) {
-        const int row = p * 32 + (tid >> 3);
+    for (int pass = 0; pass < 2; ++pass) {
+        const int row = pass * 64 + (tid >> 2);
         const uint8_t* rp = slab + row * RB;
-        float v[16];
+        // BF16: odd rows take chunk j + 4 (k ^ 1) into register group k, so
+        // the two rows a quarter-warp reads hit different banks (FP32 rows
+        // are 512 bytes, one row per quarter-warp: no conflict to avoid).
+        const int flip = kF32 ? 0 : (row & 1);
+        float v[32];
+        uint32_t pm = 0;
         if (!kF32) {
-            float a[8], b[8];
-            unpack_bf16x8(*reinterpret_cast<const uint4*>(rp + 16 * j), a);
-            unpack_bf16x8(*reinterpret_cast<const uint4*>(rp + 16 * (j + 8)), b);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) { v[i] = a[i]; v[8 + i] = b[i]; }
-        } else {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const uint4 w = *reinterpret_cast<const uint4*>(rp + 16 * (j + 8 * k));
+                const uint4 w = *reinterpret_cast<const uint4*>(rp + 16 * (j + 4 * (k ^ flip)));
+                if (kMode == kTileDual)
+                    pm = absmax_bf16x2(pm, absmax_bf16x2(absmax_bf16x2(w.x, w.y), absmax_bf16x2(w.z, w.w)));
+                float t[8];
+                unpack_bf16x8(w, t);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[8 * k + i] = t[i];
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint4 w = *reinterpret_cast<const uint4*>(rp + 16 * (j + 4 * k));
                 v[4 * k + 0] = __uint_as_float(w.x);
                 v[4 * k + 1] = __uint_as_float(w.y);
                 v[4 * k + 2] = __uint_as_float(w.z);
@@ -344,29 +434,12 @@ __global__ void __launch_bounds__(256) quantize_tile_kernel(const void* __restri
         }
         TileDiv d;
         if (kMode == kTileDual) {
-            float amax = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
-            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
-            d = tile_div(amax);
+            d = tile_div(quarter_amax<kF32>(v, pm));
             if (j == 0) s_row[(c0 >> 7) * R + r0 + row] = d.s;
         } else {
-            d = cd[0];
+            d = tile_div_from(cdiv[0][0], cdiv[1][0]);
         }
-        uint8_t* dst = q + (r0 + row) * C + c0;
-        if (!kF32) {
-            *reinterpret_cast<uint2*>(dst + 8 * j) =
-                make_uint2(e4m3x4(v[0], v[1], v[2], v[3], d), e4m3x4(v[4], v[5], v[6], v[7], d));
-            *reinterpret_cast<uint2*>(dst + 64 + 8 * j) =
-                make_uint2(e4m3x4(v[8], v[9], v[10], v[11], d), e4m3x4(v[12], v[13], v[14], v[15], d));
-        } else {
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                *reinterpret_cast<uint32_t*>(dst + 32 * k + 4 * j) =
-                    e4m3x4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3], d);
-        }
+        store_row_quarter<kF32>(q + (r0 + row) * C + c0, j, v, d, flip);
     }
 }
 
