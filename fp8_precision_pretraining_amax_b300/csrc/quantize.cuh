@@ -281,7 +281,7 @@ template <bool kF32>
 constexpr int tile_smem_bytes() { return 128 * 128 * (kF32 ? 4 : 2); }
 
 template <bool kF32, int kMode>
-__global__ void __launch_bounds__(256) quantize_tile_kernel(const void* __restrict__ x, int64_t R, int64_t C,
+__global__ void __launch_bounds__(256, 4) quantize_tile_kernel(const void* __restrict__ x, int64_t R, int64_t C,
                                                             int64_t ldx, uint8_t* __restrict__ q,
                                                             float* __restrict__ s_row, uint8_t* __restrict__ qT,
                                                             float* __restrict__ s_col) {
