@@ -166,33 +166,74 @@ int launch_tile(const void* x, int dtype, int64_t R, int64_t C, int64_t ldx, uin
     return launch_status();
 }
 
-// D is BF16 (out_f32 = false) or FP32; accumulate (FP32 only) adds into D.
+// Outputs of one GEMM launch.  d: the product, BF16 (f32 = false) or FP32,
+// may be null when only codes are wanted; accumulate (FP32 only) adds into d.
+// q / sq: row-wise 1x128 E4M3 codes [I][J] and scales [J/128][I] of the
+// BF16-rounded product (both or neither).
+struct GemmOut {
+    void* d = nullptr;
+    bool f32 = false;
+    bool accumulate = false;
+    uint8_t* q = nullptr;
+    float* sq = nullptr;
+};
+
+// n FP32 values set to v (scales of all-zero tiles).
+__global__ void fill_f32_kernel(float* p, int64_t n, float v) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i < n) p[i] = v;
+}
+
+// 2-D uint8 output [rows][cols] (dense), store boxes of 32 rows x 64 bytes
+// with 64-byte swizzle (the quantized-output epilogue's staging).
+int encode_u8_out_map(CUtensorMap* map, void* ptr, uint64_t cols, uint64_t rows) {
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols};
+    const cuuint32_t box[2] = {64, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, ptr, dims, strides, box, estr,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FP8BQ_OK : FP8BQ_ERR_CUDA;
+}
+
 template <int MODE>
-int run_gemm(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, void* D, int64_t I,
-             int64_t J, int64_t Kr, cudaStream_t stream, bool out_f32 = false, bool accumulate = false) {
+int run_gemm(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, const GemmOut& o, int64_t I,
+             int64_t J, int64_t Kr, cudaStream_t stream) {
     if (I < 0 || J < 0 || Kr < 0) return FP8BQ_ERR_SHAPE;
     if ((I % 128) || (J % 128) || (Kr % 128)) return FP8BQ_ERR_SHAPE;
     if (I >= (int64_t(1) << 31) || J >= (int64_t(1) << 31) || Kr >= (int64_t(1) << 31)) return FP8BQ_ERR_SHAPE;
     if (I == 0 || J == 0) return FP8BQ_OK;
-    if (D == nullptr) return FP8BQ_ERR_NULL;
+    if (o.d == nullptr && o.q == nullptr) return FP8BQ_ERR_NULL;
+    if ((o.q == nullptr) != (o.sq == nullptr)) return FP8BQ_ERR_NULL;
     if (Kr > 0 && (!A || !sA || !B || !sB)) return FP8BQ_ERR_NULL;
-    if (!aligned16(D)) return FP8BQ_ERR_ALIGN;
+    if ((o.d && !aligned16(o.d)) || (o.q && (!aligned16(o.q) || !aligned16(o.sq)))) return FP8BQ_ERR_ALIGN;
     if (Kr > 0 && (!aligned16(A) || !aligned16(B) || !aligned16(sA) || !aligned16(sB))) return FP8BQ_ERR_ALIGN;
     DeviceState* dev = nullptr;
     int st = probe_device(&dev);
     if (st != FP8BQ_OK) return st;
     if (Kr == 0) {
-        // empty reduction: the product is exactly zero (adding it changes nothing)
-        if (accumulate) return FP8BQ_OK;
-        return cudaMemsetAsync(D, 0, static_cast<size_t>(I) * J * (out_f32 ? 4 : 2), stream) == cudaSuccess
-                   ? FP8BQ_OK
-                   : FP8BQ_ERR_CUDA;
+        // empty reduction: the product is exactly zero (adding it changes
+        // nothing); its tiles quantize to +0 codes with scale 1
+        if (o.d && !o.accumulate &&
+            cudaMemsetAsync(o.d, 0, static_cast<size_t>(I) * J * (o.f32 ? 4 : 2), stream) != cudaSuccess)
+            return FP8BQ_ERR_CUDA;
+        if (o.q) {
+            if (cudaMemsetAsync(o.q, 0, static_cast<size_t>(I) * J, stream) != cudaSuccess) return FP8BQ_ERR_CUDA;
+            const int64_t n = I * (J / 128);
+            fill_f32_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(o.sq, n, 1.0f);
+            return launch_status();
+        }
+        return FP8BQ_OK;
     }
 
-    CUtensorMap ta, tb, td;
+    CUtensorMap ta, tb, td, tq;
     if (encode_u8_map(&ta, A, Kr, I, fp8bq::kBM) != FP8BQ_OK) return FP8BQ_ERR_CUDA;
     if (encode_u8_map(&tb, B, Kr, J, fp8bq::kBNHalf) != FP8BQ_OK) return FP8BQ_ERR_CUDA;
-    if (encode_out_map(&td, D, J, I, out_f32) != FP8BQ_OK) return FP8BQ_ERR_CUDA;
+    if (o.d && encode_out_map(&td, o.d, J, I, o.f32) != FP8BQ_OK) return FP8BQ_ERR_CUDA;
+    if (o.q && encode_u8_out_map(&tq, o.q, J, I) != FP8BQ_OK) return FP8BQ_ERR_CUDA;
+    if (!o.d) td = tq;  // unused by the kernel
+    if (!o.q) tq = td;
 
     fp8bq::GemmParams p;
     p.sA = sA;
@@ -204,15 +245,19 @@ int run_gemm(const uint8_t* A, const float* sA, const uint8_t* B, const float* s
     const int64_t tiles = ((I + fp8bq::kPairM - 1) / fp8bq::kPairM) * p.tiles_n;
     if (tiles >= (int64_t(1) << 31)) return FP8BQ_ERR_SHAPE;
     p.num_tiles = static_cast<int>(tiles);
-    p.out_f32 = out_f32 ? 1 : 0;
-    p.accumulate = accumulate ? 1 : 0;
+    p.out_f32 = o.f32 ? 1 : 0;
+    p.accumulate = o.accumulate ? 1 : 0;
+    p.out_bf16 = (o.d && !o.f32) ? 1 : 0;
+    p.out_q = o.q ? 1 : 0;
+    p.sq = o.sq;
     p.timeout_ns = kDefaultTimeoutNs;
     // persistent: one CTA pair per TPC that can hold one, never more pairs than tiles
     const int pairs = static_cast<int>(tiles < dev->max_pairs ? tiles : dev->max_pairs);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     gemm_launch_config(&cfg, attr, pairs, stream);
-    if (cudaLaunchKernelEx(&cfg, fp8bq::gemm_block_scaled_kernel<MODE>, ta, tb, td, p, dev->status) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, fp8bq::gemm_block_scaled_kernel<MODE>, ta, tb, td, tq, p, dev->status) !=
+        cudaSuccess)
         return FP8BQ_ERR_CUDA;
     return launch_status();
 }
@@ -293,24 +338,47 @@ int fp8bq_quantize_weight_block(const void* w, int dtype, int64_t N, int64_t K, 
 
 int fp8bq_gemm_fprop(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw, uint16_t* y, int64_t M,
                      int64_t N, int64_t K, fp8bq_stream_t stream) {
-    return run_gemm<fp8bq::kModeFprop>(xq, sx, wq, sw, y, M, N, K, reinterpret_cast<cudaStream_t>(stream));
+    if (y == nullptr && M > 0 && N > 0) return FP8BQ_ERR_NULL;
+    GemmOut o;
+    o.d = y;
+    return run_gemm<fp8bq::kModeFprop>(xq, sx, wq, sw, o, M, N, K, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fp8bq_gemm_fprop_q(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw, uint16_t* y,
+                       uint8_t* yq, float* sy, int64_t M, int64_t N, int64_t K, fp8bq_stream_t stream) {
+    if ((yq == nullptr || sy == nullptr) && M > 0 && N > 0) return FP8BQ_ERR_NULL;
+    GemmOut o;
+    o.d = y;
+    o.q = yq;
+    o.sq = sy;
+    return run_gemm<fp8bq::kModeFprop>(xq, sx, wq, sw, o, M, N, K, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int fp8bq_gemm_dgrad(const uint8_t* dyq, const float* sdy, const uint8_t* wqT, const float* sw, uint16_t* dx,
                      int64_t M, int64_t N, int64_t K, fp8bq_stream_t stream) {
-    return run_gemm<fp8bq::kModeDgrad>(dyq, sdy, wqT, sw, dx, M, K, N, reinterpret_cast<cudaStream_t>(stream));
+    if (dx == nullptr && M > 0 && K > 0) return FP8BQ_ERR_NULL;
+    GemmOut o;
+    o.d = dx;
+    return run_gemm<fp8bq::kModeDgrad>(dyq, sdy, wqT, sw, o, M, K, N, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int fp8bq_gemm_wgrad(const uint8_t* dyqT, const float* sdyT, const uint8_t* xqT, const float* sxT, uint16_t* dw,
                      int64_t M, int64_t N, int64_t K, fp8bq_stream_t stream) {
-    return run_gemm<fp8bq::kModeWgrad>(dyqT, sdyT, xqT, sxT, dw, N, K, M, reinterpret_cast<cudaStream_t>(stream));
+    if (dw == nullptr && N > 0 && K > 0) return FP8BQ_ERR_NULL;
+    GemmOut o;
+    o.d = dw;
+    return run_gemm<fp8bq::kModeWgrad>(dyqT, sdyT, xqT, sxT, o, N, K, M, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int fp8bq_gemm_wgrad_f32(const uint8_t* dyqT, const float* sdyT, const uint8_t* xqT, const float* sxT, float* dw,
                          int64_t M, int64_t N, int64_t K, int accumulate, fp8bq_stream_t stream) {
     if (accumulate != 0 && accumulate != 1) return FP8BQ_ERR_SHAPE;
-    return run_gemm<fp8bq::kModeWgrad>(dyqT, sdyT, xqT, sxT, dw, N, K, M, reinterpret_cast<cudaStream_t>(stream),
-                                       true, accumulate == 1);
+    if (dw == nullptr && N > 0 && K > 0) return FP8BQ_ERR_NULL;
+    GemmOut o;
+    o.d = dw;
+    o.f32 = true;
+    o.accumulate = accumulate == 1;
+    return run_gemm<fp8bq::kModeWgrad>(dyqT, sdyT, xqT, sxT, o, N, K, M, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int fp8bq_check(fp8bq_stream_t stream) {

@@ -60,6 +60,7 @@
 #include <cuda_bf16.h>
 
 #include "ptx.cuh"
+#include "quantize.cuh"
 
 namespace fp8bq {
 
@@ -92,6 +93,9 @@ struct GemmParams {
     int num_tiles;        // ceil(I / kPairM) * tiles_n
     int out_f32;          // D is FP32 (else BF16)
     int accumulate;       // FP32 D: add into it (TMA reduce-add) instead of overwriting
+    int out_bf16;         // BF16 D is written (may be 0 when only codes are wanted)
+    int out_q;            // also quantize the BF16-rounded output per 1x128 row tile
+    float* sq;            // out_q: output scales [J/128][I]
     uint64_t timeout_ns;
 };
 
@@ -175,8 +179,8 @@ __device__ __forceinline__ void cp_async_drain() { asm volatile("cp.async.wait_a
 template <int MODE>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_block_scaled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                             const __grid_constant__ CUtensorMap tmD, const GemmParams p,
-                             unsigned int* __restrict__ status) {
+                             const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmQ,
+                             const GemmParams p, unsigned int* __restrict__ status) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* smA = base;
@@ -425,29 +429,86 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int y0 = r0 + quarter * 32;
             const bool store = hv && rv;
             if (!p.out_f32) {
-                // BF16: four boxes of 32 rows x 32 columns
+                if (p.out_bf16 && !p.out_q) {
+                    // BF16 only: round while staging, four boxes of 32 x 32
 #pragma unroll
-                for (int bx = 0; bx < 4; ++bx) {
-                    // the previous box's store has finished reading the buffer
-                    if (lane == 0) bulk_wait_group_read<0>();
-                    __syncwarp();
+                    for (int bx = 0; bx < 4; ++bx) {
+                        if (lane == 0) bulk_wait_group_read<0>();
+                        __syncwarp();
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const float* a = acc + bx * 32 + j * 8;
-                        uint4 o;
-                        o.x = pack_bf16x2(a[0], a[1]);
-                        o.y = pack_bf16x2(a[2], a[3]);
-                        o.z = pack_bf16x2(a[4], a[5]);
-                        o.w = pack_bf16x2(a[6], a[7]);
-                        // 64-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ ((r >> 1) & 3)
-                        *reinterpret_cast<uint4*>(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) = o;
+                        for (int j = 0; j < 4; ++j) {
+                            const float* a = acc + bx * 32 + j * 8;
+                            *reinterpret_cast<uint4*>(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
+                                make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]),
+                                           pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7]));
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if (store) tma_store_2d(&tmD, smem_addr(stg), jh + bx * 32, y0);
+                            bulk_commit_group();
+                        }
                     }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if (store) tma_store_2d(&tmD, smem_addr(stg), jh + bx * 32, y0);
-                        bulk_commit_group();
+                } else {
+                // round to BF16 once: pk[i] holds columns 2i, 2i+1
+                uint32_t pk[64];
+#pragma unroll
+                for (int i = 0; i < 64; ++i) pk[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
+                if (p.out_bf16) {
+                    // BF16: four boxes of 32 rows x 32 columns
+#pragma unroll
+                    for (int bx = 0; bx < 4; ++bx) {
+                        // the previous box's store has finished reading the buffer
+                        if (lane == 0) bulk_wait_group_read<0>();
+                        __syncwarp();
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint32_t* w = pk + bx * 16 + j * 4;
+                            // 64-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ ((r >> 1) & 3)
+                            *reinterpret_cast<uint4*>(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
+                                make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if (store) tma_store_2d(&tmD, smem_addr(stg), jh + bx * 32, y0);
+                            bulk_commit_group();
+                        }
                     }
+                }
+                if (p.out_q) {
+                    // The thread's 128 BF16 outputs are one 1x128 row tile of
+                    // the next linear's input: quantize them exactly as the
+                    // row-wise quantizer would (codes in two 32 x 64 boxes).
+                    uint32_t m = 0;
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) m = absmax_bf16x2(m, pk[i]);
+                    const TileDiv d = tile_div(bf16x2_max_halves(m));
+#pragma unroll
+                    for (int bx = 0; bx < 2; ++bx) {
+                        if (lane == 0) bulk_wait_group_read<0>();
+                        __syncwarp();
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            float f[16];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                f[2 * i] = bf16lo(pk[bx * 32 + j * 8 + i]);
+                                f[2 * i + 1] = bf16hi(pk[bx * 32 + j * 8 + i]);
+                            }
+                            const uint2 lo = e4m3x8(f, d), hi = e4m3x8(f + 8, d);
+                            *reinterpret_cast<uint4*>(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
+                                make_uint4(lo.x, lo.y, hi.x, hi.y);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if (store) tma_store_2d(&tmQ, smem_addr(stg), jh + bx * 64, y0);
+                            bulk_commit_group();
+                        }
+                    }
+                    if (store) p.sq[static_cast<int64_t>(jh >> 7) * p.I + r0 + row] = d.s;
+                }
                 }
             } else {
                 // FP32: eight boxes of 32 rows x 16 columns, stored or added

@@ -26,8 +26,8 @@ BF16, F32 = 0, 1
 #: Names of the C-ABI entry points declared in include/fp8bq.h.
 C_FUNCTIONS = (
     "fp8bq_quantize_rowwise", "fp8bq_quantize_colwise", "fp8bq_quantize_rowcol",
-    "fp8bq_quantize_weight_block", "fp8bq_gemm_fprop", "fp8bq_gemm_dgrad", "fp8bq_gemm_wgrad",
-    "fp8bq_gemm_wgrad_f32", "fp8bq_check", "fp8bq_status_string", "fp8bq_selftest_wait_timeout",
+    "fp8bq_quantize_weight_block", "fp8bq_gemm_fprop", "fp8bq_gemm_fprop_q", "fp8bq_gemm_dgrad",
+    "fp8bq_gemm_wgrad", "fp8bq_gemm_wgrad_f32", "fp8bq_check", "fp8bq_status_string", "fp8bq_selftest_wait_timeout",
 )
 
 
@@ -44,6 +44,7 @@ def _load():
         "fp8bq_quantize_rowcol": [vp, i32, i64, i64, i64, vp, vp, vp, vp, vp],
         "fp8bq_quantize_weight_block": [vp, i32, i64, i64, i64, vp, vp, vp, vp],
         "fp8bq_gemm_fprop": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
+        "fp8bq_gemm_fprop_q": [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, vp],
         "fp8bq_gemm_dgrad": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
         "fp8bq_gemm_wgrad": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
         "fp8bq_gemm_wgrad_f32": [vp, vp, vp, vp, vp, i64, i64, i64, i32, vp],
@@ -182,6 +183,24 @@ def fp8bq_gemm_fprop(xq, sx, wq, sw, y) -> None:
                "fp8bq_gemm_fprop")
 
 
+def fp8bq_gemm_fprop_q(xq, sx, wq, sw, y, yq, sy) -> None:
+    """Fprop (as fp8bq_gemm_fprop; y may be None) whose epilogue also writes the row-wise
+    codes yq [M, N] uint8 and scales sy [N/128, M] of the BF16 output."""
+    M, K = xq.shape
+    N = wq.shape[0]
+    _need(xq, torch.uint8, (M, K), "xq")
+    _need(sx, torch.float32, (K // 128, M), "sx")
+    _need(wq, torch.uint8, (N, K), "wq")
+    _need(sw, torch.float32, (N // 128, K // 128), "sw")
+    if y is not None:
+        _need(y, torch.bfloat16, (M, N), "y")
+    _need(yq, torch.uint8, (M, N), "yq")
+    _need(sy, torch.float32, (N // 128, M), "sy")
+    with torch.cuda.device(yq.device):
+        _raise(lib.fp8bq_gemm_fprop_q(_ptr(xq), _ptr(sx), _ptr(wq), _ptr(sw), _ptr(y), _ptr(yq), _ptr(sy), M, N, K,
+                                      _stream(yq)), "fp8bq_gemm_fprop_q")
+
+
 def fp8bq_gemm_dgrad(dyq, sdy, wqT, sw, dx) -> None:
     """dX [M, K] bf16 = dYq Wq with dyq [M, N], sdy [N/128, M], wqT [K, N], sw [N/128, K/128]."""
     M, N = dyq.shape
@@ -286,6 +305,16 @@ def gemm_fprop(xq, sx, wq, sw) -> torch.Tensor:
     y = torch.empty((xq.shape[0], wq.shape[0]), dtype=torch.bfloat16, device=xq.device)
     fp8bq_gemm_fprop(xq, sx, wq, sw, y)
     return y
+
+
+def gemm_fprop_q(xq, sx, wq, sw, keep_bf16: bool = True):
+    """Returns (y or None, yq, sy)."""
+    M, N = xq.shape[0], wq.shape[0]
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device) if keep_bf16 else None
+    yq = torch.empty((M, N), dtype=torch.uint8, device=xq.device)
+    sy = torch.empty((N // 128, M), dtype=torch.float32, device=xq.device)
+    fp8bq_gemm_fprop_q(xq, sx, wq, sw, y, yq, sy)
+    return y, yq, sy
 
 
 def gemm_dgrad(dyq, sdy, wqT, sw) -> torch.Tensor:

@@ -131,6 +131,23 @@ int fp8bq_gemm_fprop(const uint8_t* xq, const float* sx, const uint8_t* wq, cons
                      uint16_t* y, int64_t M, int64_t N, int64_t K, fp8bq_stream_t stream);
 
 /*
+ * Fprop whose epilogue also quantizes its output for a following linear
+ * layer: the product is rounded to BF16 (as fp8bq_gemm_fprop writes it) and
+ * each 1x128 row tile of that BF16 output is quantized exactly as
+ * fp8bq_quantize_rowwise would (the report's FP8 recipe, section 2, applied
+ * to the next layer's input, fused into the producer so the BF16 output
+ * need not be written and read back).
+ *   y   [M][N] BF16 output, or NULL to skip writing it
+ *   yq  [M][N] E4M3 codes of the BF16 output, row-wise 1x128 tiles
+ *   sy  [N/128][M] their FP32 scales
+ * Other arguments as fp8bq_gemm_fprop.  With K == 0 the output is zero:
+ * codes +0, scales 1.
+ */
+int fp8bq_gemm_fprop_q(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw,
+                       uint16_t* y, uint8_t* yq, float* sy, int64_t M, int64_t N, int64_t K,
+                       fp8bq_stream_t stream);
+
+/*
  * Dgrad: dX[m][k] = sum_c sdy[c][m] * sw[c][k/128] * sum_{n in chunk c} D(dyq[m][n]) D(wq[n][k])
  *   dyq [M][N] codes, sdy [N/128][M]   (from fp8bq_quantize_rowwise of dY)
  *   wqT [K][N] codes (the qT output of fp8bq_quantize_weight_block),

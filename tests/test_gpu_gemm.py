@@ -261,3 +261,41 @@ def test_wgrad_f32_exact_integer_case_is_bit_exact(fb):
     assert torch.all(z == 7.0)
     fb.fp8bq_gemm_wgrad_f32(e8, e32, k8, k32, z, accumulate=False)
     assert torch.all(z == 0.0)
+
+
+# ---------------------------------------------------------------------------
+# Fprop with a quantized output (the next linear's row-wise operand)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (384, 640, 256), (1024, 2048, 512)])
+def test_fprop_q_matches_fprop_then_rowwise(fb, M, N, K):
+    """The fused epilogue quantizes the BF16-rounded product exactly as the
+    row-wise quantizer does; its BF16 output equals the plain Fprop's."""
+    rng = np.random.default_rng(5 * M + N + K)
+    xq, wq = random_codes(rng, (M, K)), random_codes(rng, (N, K))
+    sx, sw = random_scales(rng, (K // 128, M)), random_scales(rng, (N // 128, K // 128))
+    dev = [to_dev(a) for a in (xq, sx, wq, sw)]
+    y_ref = fb.gemm_fprop(*dev)
+    q_ref, s_ref = fb.quantize_rowwise(y_ref)
+    y, yq, sy = fb.gemm_fprop_q(*dev)
+    _, yq2, sy2 = fb.gemm_fprop_q(*dev, keep_bf16=False)
+    fb.check()
+    assert torch.equal(y, y_ref)
+    assert torch.equal(yq, q_ref) and torch.equal(sy, s_ref)
+    assert torch.equal(yq2, q_ref) and torch.equal(sy2, s_ref)
+    # and against the oracle: codes of the GPU's BF16 output
+    qo, so = oracle.quantize_rowwise(synth.bf16_bits(y))
+    assert np.array_equal(yq.cpu().numpy(), qo)
+    assert np.array_equal(sy.cpu().numpy().view(np.uint32), so.view(np.uint32))
+
+
+def test_fprop_q_empty_reduction(fb):
+    M, N = 256, 384
+    e8 = torch.empty((M, 0), dtype=torch.uint8, device="cuda")
+    w8 = torch.empty((N, 0), dtype=torch.uint8, device="cuda")
+    yq = torch.full((M, N), 7, dtype=torch.uint8, device="cuda")
+    sy = torch.zeros((N // 128, M), device="cuda")
+    fb.fp8bq_gemm_fprop_q(e8, torch.empty((0, M), device="cuda"), w8, torch.empty((N // 128, 0), device="cuda"),
+                          None, yq, sy)
+    fb.check()
+    assert torch.all(yq == 0) and torch.all(sy == 1.0)
