@@ -61,6 +61,10 @@ cudaError_t set_tile_smem() {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(fp8bq::quantize_tile_kernel<kF32, fp8bq::kTileWeight>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && !kF32)
+        e = cudaFuncSetAttribute(fp8bq::quantize_tile_kernel<false, fp8bq::kTileSwiglu>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 fp8bq::tile_smem_bytes<false, fp8bq::kTileSwiglu>());
     return e;
 }
 
@@ -317,6 +321,25 @@ int fp8bq_quantize_rowcol(const void* x, int dtype, int64_t M, int64_t C, int64_
     if (st != FP8BQ_OK) return st;
     return launch_tile<fp8bq::kTileDual>(x, dtype, M, C, ldx, q, s_row, qT, s_col,
                                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fp8bq_swiglu_quantize(const void* gu, int64_t M, int64_t F, int64_t ldgu, uint16_t* h, uint8_t* q,
+                          float* s_row, uint8_t* qT, float* s_col, fp8bq_stream_t stream) {
+    if (M < 0 || F < 0 || (M % 128) || (F % 128) || ldgu < 2 * F) return FP8BQ_ERR_SHAPE;
+    if (M == 0 || F == 0) return FP8BQ_OK;
+    if (!gu || !q || !s_row || !qT || !s_col) return FP8BQ_ERR_NULL;
+    if (!aligned16(gu) || !aligned16(q) || !aligned16(s_row) || !aligned16(qT) || !aligned16(s_col) ||
+        (h && !aligned16(h)) || ((ldgu * 2) % 16))
+        return FP8BQ_ERR_ALIGN;
+    if (M / 128 > 65535 || F / 128 >= (int64_t(1) << 31)) return FP8BQ_ERR_SHAPE;
+    DeviceState* dev = nullptr;
+    int st = probe_device(&dev);
+    if (st != FP8BQ_OK) return st;
+    dim3 grid(static_cast<unsigned>(F / 128), static_cast<unsigned>(M / 128));
+    fp8bq::quantize_tile_kernel<false, fp8bq::kTileSwiglu>
+        <<<grid, 256, fp8bq::tile_smem_bytes<false, fp8bq::kTileSwiglu>(), reinterpret_cast<cudaStream_t>(stream)>>>(
+            gu, M, F, ldgu, q, s_row, qT, s_col, F, h);
+    return launch_status();
 }
 
 int fp8bq_quantize_weight_block(const void* w, int dtype, int64_t N, int64_t K, int64_t ldw, uint8_t* q,

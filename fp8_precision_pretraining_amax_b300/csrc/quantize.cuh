@@ -274,17 +274,28 @@ __global__ void __launch_bounds__(256) quantize_rowwise_kernel(const void* __res
 //                slab: q [R][C], s_row [C/128][R], qT, s_col (one read of x)
 //   kTileWeight  one 128x128 block: q [R][C], qT [C][R] (optional),
 //                s_row = block scales [R/128][C/128]
+//   kTileSwiglu  BF16 only: x holds g in columns [0, C) and u in columns
+//                [uoff, uoff + C); the slab becomes H = BF16(silu(g) * u)
+//                (optionally written to h), then as kTileDual on H
 
-enum TileMode : int { kTileCol = 0, kTileDual = 1, kTileWeight = 2 };
+enum TileMode : int { kTileCol = 0, kTileDual = 1, kTileWeight = 2, kTileSwiglu = 3 };
 
-template <bool kF32>
-constexpr int tile_smem_bytes() { return 128 * 128 * (kF32 ? 4 : 2); }
+template <bool kF32, int kMode = kTileDual>
+constexpr int tile_smem_bytes() { return 128 * 128 * (kF32 ? 4 : 2) * (kMode == kTileSwiglu ? 2 : 1); }
+
+// h = silu(g) * u = g u / (1 + exp(-g)) in FP32 (expf, IEEE division and
+// product), rounded to BF16 once.
+__device__ __forceinline__ float swiglu_f32(float g, float u) {
+    return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+}
 
 template <bool kF32, int kMode>
 __global__ void __launch_bounds__(256, 4) quantize_tile_kernel(const void* __restrict__ x, int64_t R, int64_t C,
                                                             int64_t ldx, uint8_t* __restrict__ q,
                                                             float* __restrict__ s_row, uint8_t* __restrict__ qT,
-                                                            float* __restrict__ s_col) {
+                                                            float* __restrict__ s_col, int64_t uoff = 0,
+                                                            uint16_t* __restrict__ h = nullptr) {
+    static_assert(kMode != kTileSwiglu || !kF32, "the SwiGLU mode takes BF16 input");
     constexpr int E = kF32 ? 4 : 2;
     constexpr int RB = 128 * E;       // slab row pitch in shared memory (bytes)
     constexpr int CPR = RB / 16;      // 16-byte chunks per row
@@ -312,9 +323,36 @@ __global__ void __launch_bounds__(256, 4) quantize_tile_kernel(const void* __res
         const bool ok = col < C;
         const uint8_t* src = xb + ((r0 + row) * ldx + (ok ? col : c0)) * E;
         cp_async_16(sbase + row * RB + ch * 16, src, ok ? 16u : 0u);
+        if (kMode == kTileSwiglu)  // u slab right after the g slab
+            cp_async_16(sbase + 128 * RB + row * RB + ch * 16, src + uoff * E, ok ? 16u : 0u);
     }
     cp_async_wait_all();
     __syncthreads();
+
+    if (kMode == kTileSwiglu) {
+        // H = BF16(silu(g) * u), in place over the g slab (and to h)
+#pragma unroll
+        for (int k = 0; k < (128 * CPR) / 256; ++k) {
+            const int i = tid + 256 * k;
+            const int row = i / CPR, ch = i % CPR;
+            uint4* gp = reinterpret_cast<uint4*>(slab + row * RB + ch * 16);
+            const uint4 gw = *gp;
+            const uint4 uw = *reinterpret_cast<const uint4*>(slab + 128 * RB + row * RB + ch * 16);
+            const uint32_t gv[4] = {gw.x, gw.y, gw.z, gw.w}, uv[4] = {uw.x, uw.y, uw.z, uw.w};
+            uint32_t hv[4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                __nv_bfloat162 hb = __floats2bfloat162_rn(swiglu_f32(bf16lo(gv[m]), bf16lo(uv[m])),
+                                                          swiglu_f32(bf16hi(gv[m]), bf16hi(uv[m])));
+                hv[m] = *reinterpret_cast<uint32_t*>(&hb);
+            }
+            const uint4 hw = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+            *gp = hw;
+            const int64_t col = c0 + ch * 8;
+            if (h != nullptr && col < C) *reinterpret_cast<uint4*>(h + (r0 + row) * C + col) = hw;
+        }
+        __syncthreads();
+    }
 
     // ---- column view: this thread's column(s) over its row group (BF16:
     //      kept in registers for the code pass; FP32 re-reads shared memory)
@@ -415,7 +453,7 @@ __global__ void __launch_bounds__(256, 4) quantize_tile_kernel(const void* __res
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const uint4 w = *reinterpret_cast<const uint4*>(rp + 16 * (j + 4 * (k ^ flip)));
-                if (kMode == kTileDual)
+                    if (kMode == kTileDual || kMode == kTileSwiglu)
                     pm = absmax_bf16x2(pm, absmax_bf16x2(absmax_bf16x2(w.x, w.y), absmax_bf16x2(w.z, w.w)));
                 float t[8];
                 unpack_bf16x8(w, t);
@@ -433,7 +471,7 @@ __global__ void __launch_bounds__(256, 4) quantize_tile_kernel(const void* __res
             }
         }
         TileDiv d;
-        if (kMode == kTileDual) {
+        if (kMode == kTileDual || kMode == kTileSwiglu) {
             d = tile_div(quarter_amax<kF32>(v, pm));
             if (j == 0) s_row[(c0 >> 7) * R + r0 + row] = d.s;
         } else {

@@ -25,7 +25,7 @@ BF16, F32 = 0, 1
 
 #: Names of the C-ABI entry points declared in include/fp8bq.h.
 C_FUNCTIONS = (
-    "fp8bq_quantize_rowwise", "fp8bq_quantize_colwise", "fp8bq_quantize_rowcol",
+    "fp8bq_quantize_rowwise", "fp8bq_quantize_colwise", "fp8bq_quantize_rowcol", "fp8bq_swiglu_quantize",
     "fp8bq_quantize_weight_block", "fp8bq_gemm_fprop", "fp8bq_gemm_fprop_q", "fp8bq_gemm_dgrad",
     "fp8bq_gemm_wgrad", "fp8bq_gemm_wgrad_f32", "fp8bq_check", "fp8bq_status_string", "fp8bq_selftest_wait_timeout",
 )
@@ -42,6 +42,7 @@ def _load():
         "fp8bq_quantize_rowwise": [vp, i32, i64, i64, i64, vp, vp, vp],
         "fp8bq_quantize_colwise": [vp, i32, i64, i64, i64, vp, vp, vp],
         "fp8bq_quantize_rowcol": [vp, i32, i64, i64, i64, vp, vp, vp, vp, vp],
+        "fp8bq_swiglu_quantize": [vp, i64, i64, i64, vp, vp, vp, vp, vp, vp],
         "fp8bq_quantize_weight_block": [vp, i32, i64, i64, i64, vp, vp, vp, vp],
         "fp8bq_gemm_fprop": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
         "fp8bq_gemm_fprop_q": [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, vp],
@@ -153,6 +154,28 @@ def fp8bq_quantize_rowcol(x: torch.Tensor, q: torch.Tensor, s_row: torch.Tensor,
     with torch.cuda.device(x.device):
         _raise(lib.fp8bq_quantize_rowcol(_ptr(x), _dtype_code(x), M, C, ldx, _ptr(q), _ptr(s_row), _ptr(qT),
                                          _ptr(s_col), _stream(x)), "fp8bq_quantize_rowcol")
+
+
+def fp8bq_swiglu_quantize(gu: torch.Tensor, h: Optional[torch.Tensor], q: torch.Tensor, s_row: torch.Tensor,
+                          qT: torch.Tensor, s_col: torch.Tensor) -> None:
+    """gu [M, >= 2F] bf16 (g = columns [0, F), u = [F, 2F)) -> H = bf16(silu(g) u) (h, optional) and its
+    row-wise q [M, F], s_row [F/128, M] and column-wise qT [F, M], s_col [M/128, F] codes and scales."""
+    if gu.dtype != torch.bfloat16:
+        raise TypeError("gu must be bfloat16")
+    ld = _rows_input(gu, "gu")
+    M = gu.shape[0]
+    F = q.shape[1]
+    if gu.shape[1] < 2 * F:
+        raise ValueError(f"gu needs at least {2 * F} columns, got {gu.shape[1]}")
+    if h is not None:
+        _need(h, torch.bfloat16, (M, F), "h")
+    _need(q, torch.uint8, (M, F), "q")
+    _need(s_row, torch.float32, (F // 128, M), "s_row")
+    _need(qT, torch.uint8, (F, M), "qT")
+    _need(s_col, torch.float32, (M // 128, F), "s_col")
+    with torch.cuda.device(gu.device):
+        _raise(lib.fp8bq_swiglu_quantize(_ptr(gu), M, F, ld, _ptr(h), _ptr(q), _ptr(s_row), _ptr(qT), _ptr(s_col),
+                                         _stream(gu)), "fp8bq_swiglu_quantize")
 
 
 def fp8bq_quantize_weight_block(w: torch.Tensor, q: torch.Tensor, qT: Optional[torch.Tensor],
@@ -290,6 +313,19 @@ def quantize_rowcol(x: torch.Tensor):
     s_col = torch.empty((M // 128, C), dtype=torch.float32, device=x.device)
     fp8bq_quantize_rowcol(x, q, s_row, qT, s_col)
     return q, s_row, qT, s_col
+
+
+def swiglu_quantize(gu: torch.Tensor, F: int, keep_h: bool = False):
+    """Returns (h or None, q, s_row, qT, s_col) for H = silu(g) * u, g = gu[:, :F], u = gu[:, F:2F]."""
+    M = gu.shape[0]
+    d = gu.device
+    h = torch.empty((M, F), dtype=torch.bfloat16, device=d) if keep_h else None
+    q = torch.empty((M, F), dtype=torch.uint8, device=d)
+    s_row = torch.empty((F // 128, M), dtype=torch.float32, device=d)
+    qT = torch.empty((F, M), dtype=torch.uint8, device=d)
+    s_col = torch.empty((M // 128, F), dtype=torch.float32, device=d)
+    fp8bq_swiglu_quantize(gu, h, q, s_row, qT, s_col)
+    return h, q, s_row, qT, s_col
 
 
 def quantize_weight_block(w: torch.Tensor, transpose: bool = True):

@@ -110,6 +110,27 @@ int fp8bq_quantize_rowcol(const void* x, int dtype, int64_t M, int64_t C, int64_
                           uint8_t* q, float* s_row, uint8_t* qT, float* s_col, fp8bq_stream_t stream);
 
 /*
+ * SwiGLU gate fused into the quantizer of the down projection's input.  From
+ * the gate/up projection's output, h = silu(g) * u = g u / (1 + exp(-g)) is
+ * computed in FP32 and rounded to BF16 once, and that BF16 H is quantized
+ * row-wise (down projection Fprop) and column-wise (its Wgrad) exactly as
+ * fp8bq_quantize_rowcol(H) would, reading g and u once and never writing
+ * or re-reading H unless asked to (the SwiGLU MLP of the 3.8B architecture
+ * on the n1n.ai page; the report's FP8 recipe, section 2, for the down
+ * projection's input).
+ *   gu     [M][ldgu] BF16: g in columns [0, F), u in columns [F, 2F)
+ *   h      [M][F] BF16 output of H, or NULL to skip
+ *   q      [M][F] row-wise codes,     s_row [F/128][M]
+ *   qT     [F][M] column-wise codes,  s_col [M/128][F]
+ * Requires M % 128 == 0, F % 128 == 0, ldgu >= 2F, 16-byte aligned pointers
+ * and row pitch.  expf is the CUDA library's, so H may differ from a
+ * correctly rounded silu(g) u by one BF16 ulp; the codes and scales are
+ * always exactly those of the H the kernel formed.
+ */
+int fp8bq_swiglu_quantize(const void* gu, int64_t M, int64_t F, int64_t ldgu, uint16_t* h, uint8_t* q,
+                          float* s_row, uint8_t* qT, float* s_col, fp8bq_stream_t stream);
+
+/*
  * Weight quantization per 128x128 block.
  *   w      [N][K] weight of `dtype` (nn.Linear layout), row pitch ldw elements
  *   q      [N][K] E4M3 codes (Fprop operand), dense

@@ -33,6 +33,9 @@ Functions and what pins them (tests/test_oracle_*.py):
   f32_ulp / gemm_tolerance_f32  the same bound for FP32 outputs (one FP32 ulp;
                                 one more for an add into an FP32 array),
                                 pinned against numpy's spacing()
+  swiglu / swiglu_check         silu(g) * u in binary64; pinned by g = 0,
+                                the identity silu(g) - silu(-g) = g, the
+                                limits g -> +-inf, and torch's silu in float64
 """
 from __future__ import annotations
 
@@ -325,6 +328,32 @@ def gemm_check_f32(got_f32, exact, abs_sum, base=None):
     ratio = err / tol
     worst = float(np.max(ratio)) if ratio.size else 0.0
     return bool(np.all(err <= tol) and np.all(np.isfinite(got))), worst, err
+
+
+def swiglu(g_bits, u_bits) -> np.ndarray:
+    """SwiGLU gate of the down projection's input, h = silu(g) * u =
+    g * u / (1 + exp(-g)), in binary64 from BF16 inputs (bit patterns).  The
+    3.8B architecture list on the n1n.ai page names SwiGLU; the SwiGLU MLP
+    workload feeds the down projection with silu(g) * u of the gate/up output."""
+    g = bf16_bits_to_f64(g_bits)
+    u = bf16_bits_to_f64(u_bits)
+    with np.errstate(over="ignore"):
+        e = np.exp(-g)
+    # The gate is evaluated in FP32 (as a BF16 model evaluates silu): exp(-g)
+    # beyond the FP32 range is +inf there, which makes h zero.  For BF16 g
+    # this happens exactly for g <= -89 (exp(88.5) is still finite).
+    e = np.where(e > np.finfo(np.float32).max, np.inf, e)
+    return g * u / (1.0 + e)
+
+
+def swiglu_check(h_bf16_bits, g_bits, u_bits):
+    """A BF16 value of silu(g) * u computed in FP32 and rounded once must lie
+    within one BF16 ulp of the binary64 value.  Returns (ok, worst_ratio)."""
+    exact = swiglu(g_bits, u_bits)
+    got = bf16_bits_to_f64(h_bf16_bits)
+    tol = bf16_ulp(exact)
+    ratio = np.abs(got - exact) / tol
+    return bool(np.all(np.abs(got - exact) <= tol)), float(np.max(ratio)) if ratio.size else 0.0
 
 
 def gemm_check(got_bf16_bits, exact, abs_sum):

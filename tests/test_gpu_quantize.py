@@ -295,3 +295,49 @@ def test_fp32_quotients_next_to_rounding_midpoints(fb):
     _rowcol_parity(fb, x[:128].contiguous().cuda(), "midpoints rowcol")
     _colwise_parity(fb, x.t().contiguous().cuda(), "midpoints colwise")
     _weight_parity(fb, x[:128].contiguous().cuda(), "midpoints weight")
+
+
+# ---------------------------------------------------------------------------
+# SwiGLU gate fused into the down projection's quantizer
+# ---------------------------------------------------------------------------
+
+def _swiglu_case(fb, gu: torch.Tensor, F: int, what: str):
+    h, q, s_row, qT, s_col = fb.swiglu_quantize(gu, F, keep_h=True)
+    _, q2, s_row2, qT2, s_col2 = fb.swiglu_quantize(gu, F, keep_h=False)
+    fb.check()
+    g_bits = synth.bf16_bits(gu[:, :F].contiguous())
+    u_bits = synth.bf16_bits(gu[:, F:2 * F].contiguous())
+    h_bits = synth.bf16_bits(h)
+    ok, worst = oracle.swiglu_check(h_bits, g_bits, u_bits)
+    assert ok, f"{what}: H off by {worst:.3g} BF16 ulps"
+    # codes and scales are exactly those of the H the kernel formed
+    qo, so = oracle.quantize_rowwise(h_bits)
+    qTo, sco = oracle.quantize_colwise(h_bits)
+    assert_codes_equal(q.cpu().numpy(), qo, what + " row-wise codes")
+    assert_scales_equal(s_row.cpu().numpy(), so, what + " row-wise scales")
+    assert_codes_equal(qT.cpu().numpy(), qTo, what + " column-wise codes")
+    assert_scales_equal(s_col.cpu().numpy(), sco, what + " column-wise scales")
+    assert torch.equal(q, q2) and torch.equal(qT, qT2) and torch.equal(s_row, s_row2) and torch.equal(s_col, s_col2)
+    # and the same as quantizing that H with the fused row+column pass
+    q3, s3, qT3, sc3 = fb.quantize_rowcol(h)
+    assert torch.equal(q, q3) and torch.equal(qT, qT3) and torch.equal(s_row, s3) and torch.equal(s_col, sc3)
+
+
+@pytest.mark.parametrize("M,F", [(128, 128), (384, 640), (1024, 2048)])
+def test_swiglu_quantize(fb, M, F):
+    gen = synth.generator(500 + M + F)
+    gu = (synth.gaussian((M, 2 * F), 1.5, gen)).to(torch.bfloat16).cuda()
+    _swiglu_case(fb, gu, F, f"swiglu {M}x{F}")
+
+
+def test_swiglu_quantize_extremes_and_pitch(fb):
+    """Large |g| (FP32 exp overflow, silu -> 0 or g), zeros, and an input
+    whose row pitch (3F) is larger than the 2F columns g and u occupy."""
+    gen = synth.generator(71)
+    M, F = 256, 384
+    big = synth.gaussian((M, 3 * F), 1.0, gen)
+    big[:, :F][::3] *= 60.0
+    big[0, :] = 0.0
+    big[1, :F] = -1e4
+    gu = big.to(torch.bfloat16).cuda()
+    _swiglu_case(fb, gu, F, "swiglu extremes")             # ldgu = 3F > 2F
