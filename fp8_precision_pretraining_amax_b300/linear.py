@@ -68,3 +68,31 @@ class LinearFP8:
         return self.y, self.dx, self.dw
 
     LAUNCHES_PER_STEP = 6
+
+
+class SwiGLUMLPFP8:
+    """Forward of a SwiGLU MLP (x -> gate/up -> silu(g) * u -> down) on the FP8
+    path, with the SwiGLU gate fused into the down projection's quantizer.
+
+    The gate/up projection writes g and u side by side ([M, 2F] BF16); one
+    pass over them forms H = silu(g) * u and emits the down projection's
+    row-wise codes (for its Fprop) and column-wise codes (kept for its Wgrad),
+    so H itself is never written or re-read."""
+
+    def __init__(self, M: int, D: int, F: int, device="cuda"):
+        self.M, self.D, self.F = M, D, F
+        u8, f32, bf = torch.uint8, torch.float32, torch.bfloat16
+        e = lambda *shape, dt: torch.empty(shape, dtype=dt, device=device)
+        self.gate_up = LinearFP8(M, D, 2 * F, device=device)
+        self.hq, self.sh = e(M, F, dt=u8), e(F // 128, M, dt=f32)
+        self.hqT, self.shT = e(F, M, dt=u8), e(M // 128, F, dt=f32)
+        self.wdq, self.wdqT, self.swd = e(D, F, dt=u8), e(F, D, dt=u8), e(D // 128, F // 128, dt=f32)
+        self.out = e(M, D, dt=bf)
+
+    def forward(self, x: torch.Tensor, w_gate_up: torch.Tensor, w_down: torch.Tensor) -> torch.Tensor:
+        """x [M, D], w_gate_up [2F, D] (gate rows first), w_down [D, F] -> [M, D]."""
+        gu = self.gate_up.forward(x, w_gate_up)
+        fp8bq.fp8bq_swiglu_quantize(gu, None, self.hq, self.sh, self.hqT, self.shT)
+        fp8bq.fp8bq_quantize_weight_block(w_down, self.wdq, self.wdqT, self.swd)
+        fp8bq.fp8bq_gemm_fprop(self.hq, self.sh, self.wdq, self.swd, self.out)
+        return self.out
