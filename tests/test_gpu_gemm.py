@@ -299,3 +299,21 @@ def test_fprop_q_empty_reduction(fb):
                           None, yq, sy)
     fb.check()
     assert torch.all(yq == 0) and torch.all(sy == 1.0)
+
+
+@pytest.mark.slow
+def test_swiglu_mlp_config_fprop_sampled(fb):
+    """SwiGLU MLP Fprop at 16384 tokens: gate+up (2048 -> 12288) and down
+    (6144 -> 2048) whose input is H = silu(g) * u of the generated gate/up
+    (synthetic inputs quantized by the oracle), checked on sampled tiles, in
+    the launch configuration the library uses for these shapes."""
+    rng = np.random.default_rng(25)
+    gu_lin, down_lin = synth.swiglu("cuda")      # input generation only (torch FP32 matmul)
+    for lin, n in ((gu_lin, 8), (down_lin, 8)):
+        xq, sx = oracle.quantize_rowwise(host_input(lin.x))
+        wq, _, sw = oracle.quantize_weight_block(host_input(lin.w))
+        y = _fprop(fb, xq, sx, wq, sw)
+        assert y.shape == (lin.M, lin.N)
+        worst = check_gemm_tiles(y, oracle.gemm_fprop, (xq, sx, wq, sw), sample_tiles(rng, lin.M, lin.N, n),
+                                 what=f"{lin.name} fprop")
+        assert worst <= 1.0
