@@ -101,3 +101,36 @@ def test_gemm_argument_errors_are_host_side(lib):
         assert f(None, P, P, P, P, 128, 128, 128, None) == ERR_NULL
         assert f(P, P, P + 4, P, P, 128, 128, 128, None) == ERR_ALIGN
         assert f(P, P, P, P, P + 2, 128, 128, 128, None) == ERR_ALIGN
+
+
+def test_fused_and_fp32_entry_points_reject_bad_arguments_on_the_host(lib):
+    vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    rc = lib.fp8bq_quantize_rowcol
+    rc.restype, rc.argtypes = i32, [vp, i32, i64, i64, i64, vp, vp, vp, vp, vp]
+    assert rc(P, 0, 128, 200, 200, P, P, P, P, None) == ERR_SHAPE      # C not a multiple of 128
+    assert rc(P, 0, 100, 128, 128, P, P, P, P, None) == ERR_SHAPE      # M not a multiple of 128
+    assert rc(P, 0, 128, 128, 128, P, P, None, P, None) == ERR_NULL
+    assert rc(P, 0, 128, 128, 128, P, P, P + 4, P, None) == ERR_ALIGN
+    assert rc(P, 3, 128, 128, 128, P, P, P, P, None) == ERR_DTYPE
+    assert rc(P, 0, 0, 128, 128, None, None, None, None, None) == OK
+    sq = lib.fp8bq_swiglu_quantize
+    sq.restype, sq.argtypes = i32, [vp, i64, i64, i64, vp, vp, vp, vp, vp, vp]
+    assert sq(P, 128, 128, 200, None, P, P, P, P, None) == ERR_SHAPE   # ldgu < 2F
+    assert sq(P, 128, 192, 384, None, P, P, P, P, None) == ERR_SHAPE   # F not a multiple of 128
+    assert sq(P, 128, 128, 256, None, P, None, P, P, None) == ERR_NULL
+    assert sq(P, 128, 128, 256, P + 2, P, P, P, P, None) == ERR_ALIGN  # optional H misaligned
+    assert sq(P, 128, 128, 260, None, P, P, P, P, None) == ERR_ALIGN   # 520-byte pitch
+    assert sq(P, 0, 128, 256, None, None, None, None, None, None) == OK
+    wf = lib.fp8bq_gemm_wgrad_f32
+    wf.restype, wf.argtypes = i32, [vp] * 5 + [i64] * 3 + [i32, vp]
+    assert wf(P, P, P, P, P, 128, 128, 128, 2, None) == ERR_SHAPE      # accumulate must be 0 or 1
+    assert wf(P, P, P, P, P, 100, 128, 128, 0, None) == ERR_SHAPE
+    assert wf(P, P, P, P, None, 128, 128, 128, 1, None) == ERR_NULL
+    assert wf(P, P, P, P, P + 8, 128, 128, 128, 0, None) == ERR_ALIGN
+    fq = lib.fp8bq_gemm_fprop_q
+    fq.restype, fq.argtypes = i32, [vp] * 7 + [i64] * 3 + [vp]
+    assert fq(P, P, P, P, None, None, P, 128, 128, 128, None) == ERR_NULL   # codes required
+    assert fq(P, P, P, P, None, P, None, 128, 128, 128, None) == ERR_NULL   # scales required
+    assert fq(P, P, P, P, None, P, P, 128, 100, 128, None) == ERR_SHAPE
+    assert fq(P, P, P, P, None, P + 4, P, 128, 128, 128, None) == ERR_ALIGN
+    assert fq(P, P, P, P, None, P, P, 0, 128, 128, None) == OK               # empty output
