@@ -36,6 +36,15 @@ Functions and what pins them (tests/test_oracle_*.py):
   swiglu / swiglu_check         silu(g) * u in binary64; pinned by g = 0,
                                 the identity silu(g) - silu(-g) = g, the
                                 limits g -> +-inf, and torch's silu in float64
+  mx_exponent / mx_quantize_rowwise / _colwise / mx_gemm
+                                the MX variant (power-of-two scale per 1x32
+                                block): closed form of the exponent from the
+                                binary32 fields, largest element in (224, 448],
+                                2^-4 relative bound, exponent equivariance,
+                                colwise(X) == rowwise(X^T), a hand-worked block
+                                (tests/golden), brute-force Python and float64
+                                matmul of the dequantized operands, exact
+                                integer products
 """
 from __future__ import annotations
 
@@ -107,6 +116,14 @@ def _lib():
         lib.fp8bq_oracle_e4m3_encode_array.argtypes = [f32p, i64, u8p]
         lib.fp8bq_oracle_e4m3_encode_arith_array.argtypes = [f32p, i64, u8p]
         lib.fp8bq_oracle_bf16_from_double_array.argtypes = [f64p, i64, ctypes.POINTER(ctypes.c_uint16)]
+        lib.fp8bq_oracle_mx_exponent.restype = ctypes.c_int
+        lib.fp8bq_oracle_mx_exponent.argtypes = [ctypes.c_float]
+        for name in ("fp8bq_oracle_mx_quantize_rowwise", "fp8bq_oracle_mx_quantize_colwise"):
+            fn = getattr(lib, name)
+            fn.restype = None
+            fn.argtypes = [ctypes.c_void_p, ctypes.c_int, i64, i64, i64, u8p, u8p]
+        lib.fp8bq_oracle_mx_gemm.restype = None
+        lib.fp8bq_oracle_mx_gemm.argtypes = [u8p, u8p, u8p, u8p, i64, i64, i64, i64p, i64, i64p, i64, f64p, f64p]
         lib.fp8bq_oracle_num_threads.restype = ctypes.c_int
         lib.fp8bq_oracle_set_num_threads.argtypes = [ctypes.c_int]
         _lib_handle = lib
@@ -261,6 +278,63 @@ def gemm_wgrad(dyqT, sdyT, xqT, sxT, rows=None, cols=None):
     rows = np.arange(N) if rows is None else rows
     cols = np.arange(K) if cols is None else cols
     return _gemm(_lib().fp8bq_oracle_gemm_wgrad, dyqT, sdyT, xqT, sxT, M, N, K, rows, cols)
+
+
+# --------------------------------------------------------------------------
+# MX variant (power-of-two scales per 1x32 block)
+# --------------------------------------------------------------------------
+
+def mx_exponent(amax: float) -> int:
+    """Shared exponent of an MX block: the smallest E >= -127 with
+    amax <= 448 * 2^E (the tile scale amax/448 rounded up to a power of two)."""
+    return int(_lib().fp8bq_oracle_mx_exponent(float(np.float32(amax))))
+
+
+def mx_quantize_rowwise(x: np.ndarray):
+    """1x32 blocks along the last dim.  x [R, C] -> (q [R, C] uint8,
+    e8 [C/128, R, 4] uint8 holding E + 127 of block 4c + t of each row)."""
+    x, dt = _as_input(x)
+    R, C = x.shape
+    assert C % 128 == 0
+    q = np.empty((R, C), dtype=np.uint8)
+    e8 = np.empty((C // 128, R, 4), dtype=np.uint8)
+    _lib().fp8bq_oracle_mx_quantize_rowwise(x.ctypes.data, dt, R, C, C, _ptr(q, ctypes.c_uint8),
+                                            _ptr(e8, ctypes.c_uint8))
+    return q, e8
+
+
+def mx_quantize_colwise(x: np.ndarray):
+    """32x1 blocks along the first dim, emitted transposed.
+    x [M, C] -> (qT [C, M] uint8, e8 [M/128, C, 4] uint8)."""
+    x, dt = _as_input(x)
+    M, C = x.shape
+    assert M % 128 == 0
+    qT = np.empty((C, M), dtype=np.uint8)
+    e8 = np.empty((M // 128, C, 4), dtype=np.uint8)
+    _lib().fp8bq_oracle_mx_quantize_colwise(x.ctypes.data, dt, M, C, C, _ptr(qT, ctypes.c_uint8),
+                                            _ptr(e8, ctypes.c_uint8))
+    return qT, e8
+
+
+def mx_gemm(a, ea, b, eb, rows=None, cols=None):
+    """D = (2^ea A)(2^eb B)^T for K-major a [I, K], b [J, K] with exponent
+    bytes ea [K/128, I, 4], eb [K/128, J, 4].  Returns (D_exact, abs_sum),
+    float64, on the requested rows and columns."""
+    a = np.ascontiguousarray(a, dtype=np.uint8)
+    b = np.ascontiguousarray(b, dtype=np.uint8)
+    ea = np.ascontiguousarray(ea, dtype=np.uint8)
+    eb = np.ascontiguousarray(eb, dtype=np.uint8)
+    I, K = a.shape
+    J = b.shape[0]
+    rows = np.ascontiguousarray(np.arange(I) if rows is None else rows, dtype=np.int64)
+    cols = np.ascontiguousarray(np.arange(J) if cols is None else cols, dtype=np.int64)
+    val = np.empty((rows.size, cols.size), dtype=np.float64)
+    absd = np.empty((rows.size, cols.size), dtype=np.float64)
+    _lib().fp8bq_oracle_mx_gemm(_ptr(a, ctypes.c_uint8), _ptr(ea, ctypes.c_uint8), _ptr(b, ctypes.c_uint8),
+                                _ptr(eb, ctypes.c_uint8), I, J, K, _ptr(rows, ctypes.c_int64), rows.size,
+                                _ptr(cols, ctypes.c_int64), cols.size, _ptr(val, ctypes.c_double),
+                                _ptr(absd, ctypes.c_double))
+    return val, absd
 
 
 # --------------------------------------------------------------------------

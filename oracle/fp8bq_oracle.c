@@ -335,6 +335,113 @@ ORACLE_API void fp8bq_oracle_gemm_wgrad(const uint8_t* dyqT, const float* sdyT, 
     }
 }
 
+/* ------------------------------------------------------------------------ */
+/* MX variant: power-of-two scales per 1x32 block                           */
+/* ------------------------------------------------------------------------ */
+/*
+ * The variant replaces the FP32 tile scale by a power of two 2^E shared by 32
+ * consecutive elements along the reduction dimension, the block shape and
+ * scale type (an 8-bit exponent, "E8M0") of the OCP Microscaling (MX)
+ * formats specification, so that the tensor cores can apply the scales inside
+ * the MMA.  The exponent rule is this project's reading, kept as close to the
+ * layer's amax/448 rule as a power of two allows: E is the smallest integer
+ * (not below -127, the smallest E8M0 scale) with amax <= 448 * 2^E, i.e. the
+ * scale amax/448 rounded up to a power of two, so that no element saturates
+ * and the largest lands in (224, 448].  An all-zero block gets E = -127.
+ * Elements: code = E4M3(x * 2^-E), round-half-to-even; the product is exact
+ * whenever it is at least 2^-126 in magnitude, and anything smaller encodes
+ * to a signed zero either way.
+ *
+ * Storage: codes exactly like the 1x128 quantizers (row-wise [R][C], or
+ * column-wise emitted transposed [C][M]); exponent bytes E + 127 in
+ * "chunk-major" order e[C/128][R][4] (row-wise) or e[M/128][C][4]
+ * (column-wise): byte t of row r in chunk c covers elements 128c + 32t ..
+ * 128c + 32t + 31 of that row.
+ */
+
+/* The shared exponent of a block with maximum magnitude amax, found by a
+ * plain upward search from -127. */
+ORACLE_API int fp8bq_oracle_mx_exponent(float amax) {
+    int e = -127;
+    while ((double)amax > ldexp(448.0, e)) ++e;
+    return e;
+}
+
+static uint8_t mx_quantize_elem(float x, int e) {
+    double v = ldexp((double)x, -e);   /* exact in binary64 */
+    return fp8bq_oracle_e4m3_encode((float)v);
+}
+
+/* Row-wise 1x32 MX quantization: x [R][C] (pitch ldx) -> q [R][C],
+ * e8 [C/128][R][4]. */
+ORACLE_API void fp8bq_oracle_mx_quantize_rowwise(const void* x, int dtype, int64_t R, int64_t C,
+                                                 int64_t ldx, uint8_t* q, uint8_t* e8) {
+    int64_t NB = C / 32;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < R; ++r) {
+        for (int64_t b = 0; b < NB; ++b) {
+            float amax = 0.0f;
+            for (int64_t j = 0; j < 32; ++j) {
+                float a = fabsf(load_elem(x, dtype, r * ldx + b * 32 + j));
+                if (a > amax) amax = a;
+            }
+            int e = fp8bq_oracle_mx_exponent(amax);
+            e8[((b / 4) * R + r) * 4 + (b % 4)] = (uint8_t)(e + 127);
+            for (int64_t j = 0; j < 32; ++j)
+                q[r * C + b * 32 + j] = mx_quantize_elem(load_elem(x, dtype, r * ldx + b * 32 + j), e);
+        }
+    }
+}
+
+/* Column-wise 32x1 MX quantization, emitted transposed: x [M][C] (pitch ldx)
+ * -> qT [C][M] with qT[c][m] the code of x[m][c], e8 [M/128][C][4]. */
+ORACLE_API void fp8bq_oracle_mx_quantize_colwise(const void* x, int dtype, int64_t M, int64_t C,
+                                                 int64_t ldx, uint8_t* qT, uint8_t* e8) {
+    int64_t NB = M / 32;
+#pragma omp parallel for schedule(static)
+    for (int64_t c = 0; c < C; ++c) {
+        for (int64_t b = 0; b < NB; ++b) {
+            float amax = 0.0f;
+            for (int64_t i = 0; i < 32; ++i) {
+                float a = fabsf(load_elem(x, dtype, (b * 32 + i) * ldx + c));
+                if (a > amax) amax = a;
+            }
+            int e = fp8bq_oracle_mx_exponent(amax);
+            e8[((b / 4) * C + c) * 4 + (b % 4)] = (uint8_t)(e + 127);
+            for (int64_t i = 0; i < 32; ++i)
+                qT[c * M + b * 32 + i] = mx_quantize_elem(load_elem(x, dtype, (b * 32 + i) * ldx + c), e);
+        }
+    }
+}
+
+/* MX GEMM: D[i][j] = sum_k 2^(ea(i,k)) D(a[i][k]) * 2^(eb(j,k)) D(b[j][k]) for
+ * two K-major operands a [I][K], b [J][K] with exponent bytes
+ * ea [K/128][I][4], eb [K/128][J][4] (value = byte - 127).  Fprop, Dgrad and
+ * Wgrad are all this product with the operands the MX quantizers emit.
+ * Every term is exact in binary64; the sum rounds at 2^-53 relative. */
+ORACLE_API void fp8bq_oracle_mx_gemm(const uint8_t* a, const uint8_t* ea, const uint8_t* b,
+                                     const uint8_t* eb, int64_t I, int64_t J, int64_t K,
+                                     const int64_t* rows, int64_t n_rows, const int64_t* cols,
+                                     int64_t n_cols, double* out_val, double* out_abs) {
+#pragma omp parallel for schedule(dynamic)
+    for (int64_t ri = 0; ri < n_rows; ++ri) {
+        int64_t i = rows[ri];
+        for (int64_t ci = 0; ci < n_cols; ++ci) {
+            int64_t j = cols[ci];
+            double total = 0.0, total_abs = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                int64_t c = k / 128, t = (k / 32) % 4;
+                double va = ldexp(fp8bq_oracle_e4m3_decode(a[i * K + k]), (int)ea[(c * I + i) * 4 + t] - 127);
+                double vb = ldexp(fp8bq_oracle_e4m3_decode(b[j * K + k]), (int)eb[(c * J + j) * 4 + t] - 127);
+                total += va * vb;
+                total_abs += fabs(va * vb);
+            }
+            out_val[ri * n_cols + ci] = total;
+            out_abs[ri * n_cols + ci] = total_abs;
+        }
+    }
+}
+
 /* Round a binary64 value to BF16 (8 significant bits, 8 exponent bits,
  * subnormals down to 2^-133) with round-half-to-even, directly from the
  * double (no intermediate binary32 rounding).  Returns the 16-bit pattern. */
