@@ -13,6 +13,7 @@
 
 #include "fp8bq.h"
 #include "gemm.cuh"
+#include "mx.cuh"
 #include "quantize.cuh"
 
 namespace {
@@ -95,6 +96,12 @@ int probe_device(DeviceState** out) {
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
                 return FP8BQ_ERR_CUDA;
             if (set_tile_smem<false>() != cudaSuccess || set_tile_smem<true>() != cudaSuccess) return FP8BQ_ERR_CUDA;
+            if (cudaFuncSetAttribute(fp8bq::mx_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(fp8bq::kMxSmemBytes)) != cudaSuccess ||
+                cudaFuncSetAttribute(fp8bq::mx_quantize_colwise_kernel<true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     fp8bq::mx_col_smem_bytes<true>()) != cudaSuccess)
+                return FP8BQ_ERR_CUDA;
             {
                 cudaLaunchConfig_t cfg = {};
                 cudaLaunchAttribute attr[1];
@@ -402,6 +409,88 @@ int fp8bq_gemm_wgrad_f32(const uint8_t* dyqT, const float* sdyT, const uint8_t* 
     o.f32 = true;
     o.accumulate = accumulate == 1;
     return run_gemm<fp8bq::kModeWgrad>(dyqT, sdyT, xqT, sxT, o, N, K, M, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fp8bq_mx_quantize_rowwise(const void* x, int dtype, int64_t R, int64_t C, int64_t ldx, uint8_t* q,
+                              uint8_t* e8, fp8bq_stream_t stream) {
+    if (dtype != FP8BQ_BF16 && dtype != FP8BQ_F32) return FP8BQ_ERR_DTYPE;
+    if (R < 0 || C < 0 || ldx < C || (C % 128)) return FP8BQ_ERR_SHAPE;
+    if (R == 0 || C == 0) return FP8BQ_OK;
+    if (!x || !q || !e8) return FP8BQ_ERR_NULL;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(e8) || ((ldx * elem_size(dtype)) % 16)) return FP8BQ_ERR_ALIGN;
+    const int64_t nb = R * (C / 32);
+    if (nb >= (int64_t(1) << 31)) return FP8BQ_ERR_SHAPE;  // the kernel numbers blocks in 32 bits
+    DeviceState* dev = nullptr;
+    int st = probe_device(&dev);
+    if (st != FP8BQ_OK) return st;
+    const int64_t per_warp = (dtype == FP8BQ_BF16 ? 8 : 4) * fp8bq::kMxRowSteps;
+    const int64_t blocks = ((nb + per_warp - 1) / per_warp + 7) / 8;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t* ew = reinterpret_cast<uint32_t*>(e8);
+    if (dtype == FP8BQ_BF16)
+        fp8bq::mx_quantize_rowwise_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, cs>>>(x, R, C, ldx, q, ew);
+    else
+        fp8bq::mx_quantize_rowwise_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, cs>>>(x, R, C, ldx, q, ew);
+    return launch_status();
+}
+
+int fp8bq_mx_quantize_colwise(const void* x, int dtype, int64_t M, int64_t C, int64_t ldx, uint8_t* qT,
+                              uint8_t* e8, fp8bq_stream_t stream) {
+    if (dtype != FP8BQ_BF16 && dtype != FP8BQ_F32) return FP8BQ_ERR_DTYPE;
+    if (M < 0 || C < 0 || ldx < C || (M % 128) || (C % 128)) return FP8BQ_ERR_SHAPE;
+    if (M == 0 || C == 0) return FP8BQ_OK;
+    if (!x || !qT || !e8) return FP8BQ_ERR_NULL;
+    if (!aligned16(x) || !aligned16(qT) || !aligned16(e8) || ((ldx * elem_size(dtype)) % 16)) return FP8BQ_ERR_ALIGN;
+    if (M / 128 > 65535 || C / 128 >= (int64_t(1) << 31)) return FP8BQ_ERR_SHAPE;
+    DeviceState* dev = nullptr;
+    int st = probe_device(&dev);
+    if (st != FP8BQ_OK) return st;
+    dim3 grid(static_cast<unsigned>(C / 128), static_cast<unsigned>(M / 128));
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    uint16_t* eh = reinterpret_cast<uint16_t*>(e8);
+    if (dtype == FP8BQ_BF16)
+        fp8bq::mx_quantize_colwise_kernel<false>
+            <<<grid, 256, fp8bq::mx_col_smem_bytes<false>(), cs>>>(x, M, C, ldx, qT, eh);
+    else
+        fp8bq::mx_quantize_colwise_kernel<true>
+            <<<grid, 256, fp8bq::mx_col_smem_bytes<true>(), cs>>>(x, M, C, ldx, qT, eh);
+    return launch_status();
+}
+
+int fp8bq_mx_gemm(const uint8_t* a, const uint8_t* ea, const uint8_t* b, const uint8_t* eb, uint16_t* d, int64_t I,
+                  int64_t J, int64_t K, fp8bq_stream_t stream) {
+    if (I < 0 || J < 0 || K < 0 || (I % 128) || (J % 128) || (K % 128)) return FP8BQ_ERR_SHAPE;
+    if (I >= (int64_t(1) << 31) || J >= (int64_t(1) << 31) || K >= (int64_t(1) << 31)) return FP8BQ_ERR_SHAPE;
+    if (I == 0 || J == 0) return FP8BQ_OK;
+    if (!d) return FP8BQ_ERR_NULL;
+    if (K > 0 && (!a || !ea || !b || !eb)) return FP8BQ_ERR_NULL;
+    if (!aligned16(d)) return FP8BQ_ERR_ALIGN;
+    if (K > 0 && (!aligned16(a) || !aligned16(ea) || !aligned16(b) || !aligned16(eb))) return FP8BQ_ERR_ALIGN;
+    DeviceState* dev = nullptr;
+    int st = probe_device(&dev);
+    if (st != FP8BQ_OK) return st;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if (K == 0) {  // empty reduction: exact zeros
+        return cudaMemsetAsync(d, 0, static_cast<size_t>(I) * J * 2, cs) == cudaSuccess ? FP8BQ_OK : FP8BQ_ERR_CUDA;
+    }
+    CUtensorMap ta, tb, td;
+    if (encode_u8_map(&ta, a, K, I, fp8bq::kMxBM) != FP8BQ_OK) return FP8BQ_ERR_CUDA;
+    if (encode_u8_map(&tb, b, K, J, fp8bq::kMxBN) != FP8BQ_OK) return FP8BQ_ERR_CUDA;
+    if (encode_out_map(&td, d, J, I, false) != FP8BQ_OK) return FP8BQ_ERR_CUDA;
+    fp8bq::MxParams p;
+    p.ea = reinterpret_cast<const uint32_t*>(ea);
+    p.eb = reinterpret_cast<const uint32_t*>(eb);
+    p.I = static_cast<int>(I);
+    p.J = static_cast<int>(J);
+    p.KC = static_cast<int>(K / 128);
+    p.tiles_n = static_cast<int>((J + fp8bq::kMxBN - 1) / fp8bq::kMxBN);
+    const int64_t tiles = (I / fp8bq::kMxBM) * p.tiles_n;
+    if (tiles >= (int64_t(1) << 31)) return FP8BQ_ERR_SHAPE;
+    p.num_tiles = static_cast<int>(tiles);
+    p.timeout_ns = kDefaultTimeoutNs;
+    const int grid = static_cast<int>(tiles < dev->sms ? tiles : dev->sms);  // persistent, one CTA per SM
+    fp8bq::mx_gemm_kernel<<<grid, fp8bq::kMxThreads, fp8bq::kMxSmemBytes, cs>>>(ta, tb, td, p, dev->status);
+    return launch_status();
 }
 
 int fp8bq_check(fp8bq_stream_t stream) {

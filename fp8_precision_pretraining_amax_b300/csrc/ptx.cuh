@@ -253,6 +253,50 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// 32 lanes x 4 (or 8) consecutive 32-bit columns: thread i of the warp writes
+// TMEM lane (lane_base + i), columns [col, col + 4) (or + 8).  Asynchronous
+// until tmem_wait_st().
+__device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2,
+                                                  uint32_t v3) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v0), "r"(v1),
+                 "r"(v2), "r"(v3)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&v)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Instruction descriptor of tcgen05.mma.kind::mxf8f6f4.block_scale for
+// E4M3 x E4M3 with 8-bit power-of-two (E8M0) scale factors, both operands
+// K-major, dense: B scale-factor id (bits 4-5), A/B format E4M3 (bits 7-9,
+// 10-12 = 0), N >> 3 (bits 17-22), scale format E8M0 (bit 23 = 1), M >> 4
+// (bits 24-28), A scale-factor id (bits 29-30).  The id picks the byte of
+// each 32-bit scale-factor cell in TMEM, i.e. which of four consecutive
+// 32-element K blocks this K = 32 step uses.
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3(int M, int N, int sf_id) {
+    return (static_cast<uint32_t>(sf_id) << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) |
+           (static_cast<uint32_t>(M >> 4) << 24) | (static_cast<uint32_t>(sf_id) << 29);
+}
+
+// D[tmem] (+)= (SFA . A[smem]) * (SFB . B[smem])^T, one M x N x 32 step with a
+// power-of-two scale per row of A and per row of B for these 32 K values
+// (one CTA).  sfa / sfb are the TMEM addresses of the scale-factor cells.
+__device__ __forceinline__ void mma_mx_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+}
+
 // Empty volatile statement that "redefines" 32 registers: placed after
 // tmem_wait_ld(), it keeps every use of registers filled by an asynchronous
 // tcgen05.ld from being scheduled before the wait.

@@ -27,7 +27,8 @@ BF16, F32 = 0, 1
 C_FUNCTIONS = (
     "fp8bq_quantize_rowwise", "fp8bq_quantize_colwise", "fp8bq_quantize_rowcol", "fp8bq_swiglu_quantize",
     "fp8bq_quantize_weight_block", "fp8bq_gemm_fprop", "fp8bq_gemm_fprop_q", "fp8bq_gemm_dgrad",
-    "fp8bq_gemm_wgrad", "fp8bq_gemm_wgrad_f32", "fp8bq_check", "fp8bq_status_string", "fp8bq_selftest_wait_timeout",
+    "fp8bq_gemm_wgrad", "fp8bq_gemm_wgrad_f32", "fp8bq_mx_quantize_rowwise", "fp8bq_mx_quantize_colwise",
+    "fp8bq_mx_gemm", "fp8bq_check", "fp8bq_status_string", "fp8bq_selftest_wait_timeout",
 )
 
 
@@ -49,6 +50,9 @@ def _load():
         "fp8bq_gemm_dgrad": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
         "fp8bq_gemm_wgrad": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
         "fp8bq_gemm_wgrad_f32": [vp, vp, vp, vp, vp, i64, i64, i64, i32, vp],
+        "fp8bq_mx_quantize_rowwise": [vp, i32, i64, i64, i64, vp, vp, vp],
+        "fp8bq_mx_quantize_colwise": [vp, i32, i64, i64, i64, vp, vp, vp],
+        "fp8bq_mx_gemm": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
         "fp8bq_check": [vp],
         "fp8bq_selftest_wait_timeout": [i64, vp],
     }
@@ -266,6 +270,42 @@ def fp8bq_gemm_wgrad_f32(dyqT, sdyT, xqT, sxT, dw, accumulate: bool = False) -> 
                                         1 if accumulate else 0, _stream(dw)), "fp8bq_gemm_wgrad_f32")
 
 
+def fp8bq_mx_quantize_rowwise(x: torch.Tensor, q: torch.Tensor, e8: torch.Tensor) -> None:
+    """MX variant.  x [R, C] bf16/f32 -> q [R, C] uint8 codes, e8 [C/128, R, 4] uint8 exponents (E + 127)."""
+    ldx = _rows_input(x, "x")
+    R, C = x.shape
+    _need(q, torch.uint8, (R, C), "q")
+    _need(e8, torch.uint8, (C // 128, R, 4), "e8")
+    with torch.cuda.device(x.device):
+        _raise(lib.fp8bq_mx_quantize_rowwise(_ptr(x), _dtype_code(x), R, C, ldx, _ptr(q), _ptr(e8), _stream(x)),
+               "fp8bq_mx_quantize_rowwise")
+
+
+def fp8bq_mx_quantize_colwise(x: torch.Tensor, qT: torch.Tensor, e8: torch.Tensor) -> None:
+    """MX variant.  x [M, C] bf16/f32 -> qT [C, M] uint8 codes (32x1 blocks), e8 [M/128, C, 4] uint8."""
+    ldx = _rows_input(x, "x")
+    M, C = x.shape
+    _need(qT, torch.uint8, (C, M), "qT")
+    _need(e8, torch.uint8, (M // 128, C, 4), "e8")
+    with torch.cuda.device(x.device):
+        _raise(lib.fp8bq_mx_quantize_colwise(_ptr(x), _dtype_code(x), M, C, ldx, _ptr(qT), _ptr(e8), _stream(x)),
+               "fp8bq_mx_quantize_colwise")
+
+
+def fp8bq_mx_gemm(a, ea, b, eb, d) -> None:
+    """MX variant.  d [I, J] bf16 = (2^ea a)(2^eb b)^T: a [I, K], ea [K/128, I, 4], b [J, K], eb [K/128, J, 4]."""
+    I, K = a.shape
+    J = b.shape[0]
+    _need(a, torch.uint8, (I, K), "a")
+    _need(ea, torch.uint8, (K // 128, I, 4), "ea")
+    _need(b, torch.uint8, (J, K), "b")
+    _need(eb, torch.uint8, (K // 128, J, 4), "eb")
+    _need(d, torch.bfloat16, (I, J), "d")
+    with torch.cuda.device(d.device):
+        _raise(lib.fp8bq_mx_gemm(_ptr(a), _ptr(ea), _ptr(b), _ptr(eb), _ptr(d), I, J, K, _stream(d)),
+               "fp8bq_mx_gemm")
+
+
 def fp8bq_check(device=None) -> None:
     """Synchronize the current stream and raise if a kernel reported a device-side timeout."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
@@ -369,6 +409,30 @@ def gemm_wgrad_f32(dyqT, sdyT, xqT, sxT) -> torch.Tensor:
     dw = torch.empty((dyqT.shape[0], xqT.shape[0]), dtype=torch.float32, device=dyqT.device)
     fp8bq_gemm_wgrad_f32(dyqT, sdyT, xqT, sxT, dw)
     return dw
+
+
+def mx_quantize_rowwise(x: torch.Tensor) -> Tuple[torch.Tensor, torch.Tensor]:
+    """MX variant: returns (q [R, C], e8 [C/128, R, 4])."""
+    R, C = x.shape
+    q = torch.empty((R, C), dtype=torch.uint8, device=x.device)
+    e8 = torch.empty((C // 128, R, 4), dtype=torch.uint8, device=x.device)
+    fp8bq_mx_quantize_rowwise(x, q, e8)
+    return q, e8
+
+
+def mx_quantize_colwise(x: torch.Tensor) -> Tuple[torch.Tensor, torch.Tensor]:
+    """MX variant: returns (qT [C, M], e8 [M/128, C, 4])."""
+    M, C = x.shape
+    qT = torch.empty((C, M), dtype=torch.uint8, device=x.device)
+    e8 = torch.empty((M // 128, C, 4), dtype=torch.uint8, device=x.device)
+    fp8bq_mx_quantize_colwise(x, qT, e8)
+    return qT, e8
+
+
+def mx_gemm(a, ea, b, eb) -> torch.Tensor:
+    d = torch.empty((a.shape[0], b.shape[0]), dtype=torch.bfloat16, device=a.device)
+    fp8bq_mx_gemm(a, ea, b, eb, d)
+    return d
 
 
 check = fp8bq_check

@@ -204,6 +204,63 @@ int fp8bq_gemm_wgrad(const uint8_t* dyqT, const float* sdyT, const uint8_t* xqT,
 int fp8bq_gemm_wgrad_f32(const uint8_t* dyqT, const float* sdyT, const uint8_t* xqT, const float* sxT,
                          float* dw, int64_t M, int64_t N, int64_t K, int accumulate, fp8bq_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * MX variant: one power-of-two scale per 1x32 block
+ *
+ * A variant of the layer whose scales the tensor cores apply inside the MMA
+ * (tcgen05.mma.kind::mxf8f6f4.block_scale), so no per-chunk promotion runs on
+ * the CUDA cores.  Block shape and scale type are those of the OCP
+ * Microscaling (MX) formats specification: 32 consecutive elements along the
+ * reduction dimension share a scale 2^E stored as the byte E + 127 ("E8M0").
+ * E is the layer's amax/448 scale rounded up to a power of two: the smallest
+ * integer >= -127 with amax <= 448 * 2^E (so nothing saturates; an all-zero
+ * block gets E = -127).  code = E4M3 of x * 2^-E, round half to even.  This
+ * is a different numerical contract from the FP32-scale entry points above;
+ * its codes and exponents are not interchangeable with theirs.
+ *
+ * Exponent arrays are uint8 and chunk-major: byte t of the 32-bit word for
+ * row r and 128-element reduction chunk c, e[(c * rows + r) * 4 + t], is the
+ * exponent of elements 128c + 32t .. 128c + 32t + 31 of that row.
+ * ------------------------------------------------------------------------ */
+
+/*
+ * Row-wise MX quantization (1x32 blocks along C).
+ *   x   [R][C] BF16 or FP32, row pitch ldx elements (ldx >= C)
+ *   q   [R][C] uint8 E4M3 codes, dense
+ *   e8  [C/128][R][4] uint8 exponents (E + 127)
+ * Requires C % 128 == 0 and R * C / 32 < 2^31.  One read of x.
+ * Fprop operands: X [M][K] and W [N][K]; Dgrad's left operand dY [M][N].
+ */
+int fp8bq_mx_quantize_rowwise(const void* x, int dtype, int64_t R, int64_t C, int64_t ldx, uint8_t* q,
+                              uint8_t* e8, fp8bq_stream_t stream);
+
+/*
+ * Column-wise MX quantization (32x1 blocks along M), emitted transposed.
+ *   x   [M][C] BF16 or FP32, row pitch ldx elements (ldx >= C)
+ *   qT  [C][M] uint8 codes, qT[c][m] the code of x[m][c]
+ *   e8  [M/128][C][4] uint8 exponents
+ * Requires M % 128 == 0, C % 128 == 0, M / 128 <= 65535.
+ * Dgrad's right operand (W [N][K] -> [K][N]) and both Wgrad operands
+ * (dY [M][N] -> [N][M], X [M][K] -> [K][M]).
+ */
+int fp8bq_mx_quantize_colwise(const void* x, int dtype, int64_t M, int64_t C, int64_t ldx, uint8_t* qT,
+                              uint8_t* e8, fp8bq_stream_t stream);
+
+/*
+ * MX GEMM: d[i][j] = BF16( sum_k 2^(ea(i,k)-127) D(a[i][k]) * 2^(eb(j,k)-127) D(b[j][k]) )
+ * for two K-major operands as the MX quantizers emit them:
+ *   a   [I][K] codes, ea [K/128][I][4] exponents
+ *   b   [J][K] codes, eb [K/128][J][4] exponents
+ *   d   [I][J] BF16 output, dense
+ * Fprop: (a, b) = (rowwise X, rowwise W), I = M, J = N, K = K.
+ * Dgrad: (rowwise dY, colwise W), I = M, J = K, reduction N.
+ * Wgrad: (colwise dY, colwise X), I = N, J = K, reduction M.
+ * The products accumulate in FP32 in tensor memory; the acceptance bound of
+ * the FP32-scale GEMMs applies.  Requires I, J, K % 128 == 0 and each < 2^31.
+ */
+int fp8bq_mx_gemm(const uint8_t* a, const uint8_t* ea, const uint8_t* b, const uint8_t* eb, uint16_t* d,
+                  int64_t I, int64_t J, int64_t K, fp8bq_stream_t stream);
+
 /*
  * Synchronize `stream`, then read and clear the current device's status word.
  * Returns FP8BQ_OK, FP8BQ_ERR_TIMEOUT if a kernel launched since the last

@@ -134,3 +134,27 @@ def test_fused_and_fp32_entry_points_reject_bad_arguments_on_the_host(lib):
     assert fq(P, P, P, P, None, P, P, 128, 100, 128, None) == ERR_SHAPE
     assert fq(P, P, P, P, None, P + 4, P, 128, 128, 128, None) == ERR_ALIGN
     assert fq(P, P, P, P, None, P, P, 0, 128, 128, None) == OK               # empty output
+
+
+def test_mx_entry_points_reject_bad_arguments_on_the_host(lib):
+    vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    for name in ("fp8bq_mx_quantize_rowwise", "fp8bq_mx_quantize_colwise"):
+        f = getattr(lib, name)
+        f.restype, f.argtypes = i32, [vp, i32, i64, i64, i64, vp, vp, vp]
+        assert f(P, 5, 128, 128, 128, P, P, None) == ERR_DTYPE
+        assert f(P, 0, 128, 96, 96, P, P, None) == ERR_SHAPE         # C not a multiple of 128
+        assert f(P, 0, 128, 256, 128, P, P, None) == ERR_SHAPE       # pitch < width
+        assert f(P, 0, 0, 128, 128, None, None, None) == OK          # empty: no-op
+        assert f(P, 0, 128, 128, 128, P, None, None) == ERR_NULL
+        assert f(P, 0, 128, 128, 128, P, P + 4, None) == ERR_ALIGN
+        assert f(P, 1, 128, 128, 130, P, P, None) == ERR_ALIGN       # 520-byte pitch
+    g = lib.fp8bq_mx_quantize_colwise
+    assert g(P, 0, 96, 128, 128, P, P, None) == ERR_SHAPE            # M not a multiple of 128
+    m = lib.fp8bq_mx_gemm
+    m.restype, m.argtypes = i32, [vp] * 5 + [i64] * 3 + [vp]
+    assert m(P, P, P, P, P, 128, 128, 100, None) == ERR_SHAPE
+    assert m(P, P, P, P, P, 128, 192, 128, None) == ERR_SHAPE
+    assert m(P, P, P, P, P, 0, 128, 128, None) == OK                # empty output
+    assert m(P, P, P, P, None, 128, 128, 128, None) == ERR_NULL
+    assert m(P, None, P, P, P, 128, 128, 128, None) == ERR_NULL
+    assert m(P, P, P, P + 4, P, 128, 128, 128, None) == ERR_ALIGN
