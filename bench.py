@@ -1,7 +1,7 @@
 """Benchmark of the block-scaled FP8 linear layer on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--tokens M]
-                    [--impl reference]
+                    [--impl reference] [--variant mx]
 
 One step is one pass of the whole hot path over one batch: for every linear
 of the workload, the weight-block quantizer (with the transposed copy), one
@@ -24,6 +24,11 @@ against the FP8 tensor peak, the quantizers against HBM), the same metric
 end to end through the Python API with pinned host buffers (host->device
 copies of X, W, dY and device->host copies of Y, dX, dW inside the timed
 region), and the CPU oracle timed on a bounded sample on the host cores.
+
+--variant mx times the MX variant of the same step instead: every operand
+quantized with a power-of-two scale per 1x32 block along its GEMM's reduction
+dimension (row-wise and column-wise passes over X, W and dY) and the three
+GEMMs on the block-scaled MMA, which applies the scales itself.
 
 Multi-GPU (torchrun): data parallel with weak scaling.  Every rank runs the
 step on its own batch of the workload's size; Fprop and Dgrad need nothing
@@ -49,6 +54,11 @@ METRIC = "FP8 block-scaled GEMM TFLOP/s (incl. quantize) and % of B300 FP8 peak"
 UNIT = "TFLOP/s"
 TOKENS = {"layer_3p8b": 32768, "qkv_1p7b": 8192, "tiny": 256}
 FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 / 2.25 PFLOP/s)
+VARIANTS = {
+    "fp32-scale": "FP32 scale amax/448 per 1x128 tile (X, dY) and 128x128 block (W); per-128-chunk promotion",
+    "mx": ("MX variant: power-of-two (E8M0) scale per 1x32 block along each GEMM's reduction dim, "
+           "applied inside the block-scaled MMA; every operand quantized in both layouts"),
+}
 
 
 def parse_args(argv=None):
@@ -60,6 +70,9 @@ def parse_args(argv=None):
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the token count M of the workload (e.g. a smaller case for ncu)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--variant", default="fp32-scale", choices=["fp32-scale", "mx"],
+                    help="fp32-scale: the layer's FP32 amax/448 scales per 1x128 tile / 128x128 block with "
+                         "per-chunk promotion; mx: power-of-two scale per 1x32 block applied inside the MMA")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args(argv)
@@ -190,11 +203,13 @@ def peaks():
         return {"hbm_gbs": 6400.0, "bf16_burst": 1800.0, "bf16_sustained": 1400.0, "source": "fallback"}
 
 
-def gemm_traffic_record():
+def gemm_traffic_record(variant="fp32-scale"):
     """DRAM bytes per GEMM launch from the committed ncu summary; valid only
     while the kernel source is unchanged (its sha256 is recorded there)."""
-    src = os.path.join(ROOT, "fp8_precision_pretraining_amax_b300", "csrc", "gemm.cuh")
-    rec = os.path.join(ROOT, "profiles", "gemm_block_scaled_layer_3p8b_traffic.txt")
+    name, key = {"fp32-scale": ("gemm.cuh", "gemm_block_scaled_layer_3p8b_traffic.txt"),
+                 "mx": ("mx.cuh", "mx_gemm_layer_3p8b_traffic.txt")}[variant]
+    src = os.path.join(ROOT, "fp8_precision_pretraining_amax_b300", "csrc", name)
+    rec = os.path.join(ROOT, "profiles", key)
     try:
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
         kv = {}
@@ -202,7 +217,7 @@ def gemm_traffic_record():
             if ":" in line and not line.startswith("#"):
                 k, v = line.split(":", 1)
                 kv[k.strip()] = v.strip()
-        return kv if kv.get("gemm_cuh_sha256") == sha else None
+        return kv if kv.get(name.replace(".", "_") + "_sha256") == sha else None
     except OSError:
         return None
 
@@ -229,17 +244,36 @@ def step_launches(fp8bq, L, lin):
     ]
 
 
+def step_launches_mx(fp8bq, L, lin):
+    """The MX variant's 9 launches per linear, in step order.  Quantizer bytes:
+    BF16 in, one code byte and 1/32 exponent byte per element and layout."""
+    M, K, N = L.M, L.K, L.N
+    one = lambda R, C: 2 * R * C + R * C + R * C // 32
+    return [
+        ("quant_mx_rowwise", one(N, K), lambda: fp8bq.fp8bq_mx_quantize_rowwise(lin.w, L.wq, L.ew)),
+        ("quant_mx_colwise", one(N, K), lambda: fp8bq.fp8bq_mx_quantize_colwise(lin.w, L.wqT, L.ewT)),
+        ("quant_mx_rowwise", one(M, K), lambda: fp8bq.fp8bq_mx_quantize_rowwise(lin.x, L.xq, L.ex)),
+        ("quant_mx_colwise", one(M, K), lambda: fp8bq.fp8bq_mx_quantize_colwise(lin.x, L.xqT, L.exT)),
+        ("gemm_mx_fprop", 2 * M * N * K, lambda: fp8bq.fp8bq_mx_gemm(L.xq, L.ex, L.wq, L.ew, L.y)),
+        ("quant_mx_rowwise", one(M, N), lambda: fp8bq.fp8bq_mx_quantize_rowwise(lin.dy, L.dyq, L.edy)),
+        ("quant_mx_colwise", one(M, N), lambda: fp8bq.fp8bq_mx_quantize_colwise(lin.dy, L.dyqT, L.edyT)),
+        ("gemm_mx_dgrad", 2 * M * N * K, lambda: fp8bq.fp8bq_mx_gemm(L.dyq, L.edy, L.wqT, L.ewT, L.dx)),
+        ("gemm_mx_wgrad", 2 * M * N * K, lambda: fp8bq.fp8bq_mx_gemm(L.dyqT, L.edyT, L.xqT, L.exT, L.dw)),
+    ]
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     from fp8_precision_pretraining_amax_b300 import fp8bq
-    from fp8_precision_pretraining_amax_b300.linear import LinearFP8
+    from fp8_precision_pretraining_amax_b300.linear import LinearFP8, LinearMX
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     shapes = workload_shapes(args.workload, args.tokens)
     lins = make_inputs(args.workload, dev, args.tokens)
-    layers = [LinearFP8(l.M, l.K, l.N, device=dev) for l in lins]
-    plan = [step_launches(fp8bq, L, lin) for L, lin in zip(layers, lins)]
+    mx = args.variant == "mx"
+    layers = [(LinearMX if mx else LinearFP8)(l.M, l.K, l.N, device=dev) for l in lins]
+    plan = [(step_launches_mx if mx else step_launches)(fp8bq, L, lin) for L, lin in zip(layers, lins)]
     if world > 1:
         # data parallel: each rank's batch gives a partial dW; the ranks sum
         # them (NCCL all-reduce of the BF16 dW of every linear, each step)
@@ -319,7 +353,7 @@ def run_ours(args, rank, world, local_rank):
     g_ms, g_fl, g_n = sum(v["ms"] for v in gk), sum(v["work"] for v in gk), sum(v["launches"] for v in gk)
     q_ms, q_by = sum(v["ms"] for v in qk), sum(v["work"] for v in qk)
     achieved = g_fl / (g_ms * 1e-3) / 1e12
-    tr = gemm_traffic_record()
+    tr = gemm_traffic_record(args.variant)
     traffic = None
     if tr is not None and tr.get("workload") == args.workload and args.tokens in (None, TOKENS[args.workload]):
         traffic = float(tr["dram_bytes_per_launch"])
@@ -337,16 +371,21 @@ def run_ours(args, rank, world, local_rank):
                                "frac_of_hbm": q_by / (q_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
                                "ms_per_step": q_ms / args.steps}
     cfg = workload_config(args.workload, args.tokens)
+    cfg["variant"] = VARIANTS[args.variant]
     cfg["parallelism"] = (f"data parallel x{world}: own batch per rank, dW all-reduced each step"
                           if world > 1 else "single GPU")
     cfg["l2"] = "inputs larger than L2 (no flush)" if args.workload != "tiny" else "inputs fit in L2"
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32 accumulate -> bf16", "data": "synthetic",
+        "vs_baseline": None,
+        "dtype": ("e4m3 (e8m0 block scales) x e4m3 -> f32 accumulate -> bf16" if mx
+                  else "e4m3 x e4m3 -> f32 accumulate -> bf16"), "data": "synthetic",
         "config": cfg,
         "pct_of_fp8_peak": 100.0 * value / fp8_sus,
-        "roofline": {"bound": "tensor", "kernel": "gemm_block_scaled_kernel (Fprop/Dgrad/Wgrad)",
+        "roofline": {"bound": "tensor",
+                     "kernel": ("mx_gemm_kernel (Fprop/Dgrad/Wgrad)" if mx
+                                else "gemm_block_scaled_kernel (Fprop/Dgrad/Wgrad)"),
                      "achieved": achieved, "peak": fp8_sus, "unit": "TFLOP/s", "frac": achieved / fp8_sus,
                      "traffic": traffic,
                      "peak_note": (f"FP8 = 2 x {pk['source']} sustained cuBLAS bf16 ({pk['bf16_sustained']} "
@@ -359,7 +398,7 @@ def run_ours(args, rank, world, local_rank):
     if e2e is not None:
         out["e2e"] = e2e
     if not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(lins)
+        out["cpu_baseline"] = cpu_baseline(lins, variant=args.variant)
     return out
 
 
@@ -430,8 +469,8 @@ def run_e2e(args, lins, layers, dev, flops, world, barrier):
         dt = float(t.item())
     return {"value": flops * world * steps / dt / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": 1e3 * dt / steps,
-            "path": ("pinned host -> device copies, LinearFP8.step (C-ABI), device -> pinned host copies; "
-                     "copies of neighbouring linears overlap compute on separate streams")}
+            "path": (f"pinned host -> device copies, {type(layers[0]).__name__}.step (C-ABI), device -> pinned "
+                     "host copies; copies of neighbouring linears overlap compute on separate streams")}
 
 
 # ---------------------------------------------------------------------------
@@ -453,7 +492,7 @@ def host_slices(lins, tile):
     return out
 
 
-def oracle_sample(slices, tile):
+def oracle_sample(slices, tile, variant="fp32-scale"):
     """Time the oracle on a bounded sample of one step and extrapolate.
 
     For each linear: quantize the operand slices that one tile x tile output
@@ -466,31 +505,47 @@ def oracle_sample(slices, tile):
     q_time = g_time = 0.0
     q_elems = g_macs = full_q = full_macs = 0
     for (_, M, K, N), (xr, xc, wr, wc, dyr, dyc) in slices:
-        full_q += 2 * M * K + 2 * M * N + N * K  # row-wise X, dY; column-wise dY, X; weight
         full_macs += 3 * M * N * K
-        t = time.perf_counter()
-        xq, sx = oracle.quantize_rowwise(xr)
-        wq, _, sw = oracle.quantize_weight_block(wr)
-        dyq, sdy = oracle.quantize_rowwise(dyr)
-        wq2, _, sw2 = oracle.quantize_weight_block(wc)
-        dyqT, sdyT = oracle.quantize_colwise(dyc)
-        xqT, sxT = oracle.quantize_colwise(xc)
-        q_time += time.perf_counter() - t
-        q_elems += xr.size + wr.size + dyr.size + wc.size + dyc.size + xc.size
         idx = np.arange(tile)
-        t = time.perf_counter()
-        oracle.gemm_fprop(xq, sx, wq, sw, rows=idx, cols=idx)
-        oracle.gemm_dgrad(dyq, sdy, wq2, sw2, rows=idx, cols=idx)
-        oracle.gemm_wgrad(dyqT, sdyT, xqT, sxT, rows=idx, cols=idx)
-        g_time += time.perf_counter() - t
+        if variant == "mx":
+            full_q += 2 * M * K + 2 * M * N + 2 * N * K  # every operand in both layouts
+            t = time.perf_counter()
+            xq = oracle.mx_quantize_rowwise(xr)
+            wq = oracle.mx_quantize_rowwise(wr)
+            dyq = oracle.mx_quantize_rowwise(dyr)
+            wqT = oracle.mx_quantize_colwise(wc)
+            dyqT = oracle.mx_quantize_colwise(dyc)
+            xqT = oracle.mx_quantize_colwise(xc)
+            q_time += time.perf_counter() - t
+            t = time.perf_counter()
+            oracle.mx_gemm(*xq, *wq, rows=idx, cols=idx)
+            oracle.mx_gemm(*dyq, *wqT, rows=idx, cols=idx)
+            oracle.mx_gemm(*dyqT, *xqT, rows=idx, cols=idx)
+            g_time += time.perf_counter() - t
+        else:
+            full_q += 2 * M * K + 2 * M * N + N * K  # row-wise X, dY; column-wise dY, X; weight
+            t = time.perf_counter()
+            xq, sx = oracle.quantize_rowwise(xr)
+            wq, _, sw = oracle.quantize_weight_block(wr)
+            dyq, sdy = oracle.quantize_rowwise(dyr)
+            wq2, _, sw2 = oracle.quantize_weight_block(wc)
+            dyqT, sdyT = oracle.quantize_colwise(dyc)
+            xqT, sxT = oracle.quantize_colwise(xc)
+            q_time += time.perf_counter() - t
+            t = time.perf_counter()
+            oracle.gemm_fprop(xq, sx, wq, sw, rows=idx, cols=idx)
+            oracle.gemm_dgrad(dyq, sdy, wq2, sw2, rows=idx, cols=idx)
+            oracle.gemm_wgrad(dyqT, sdyT, xqT, sxT, rows=idx, cols=idx)
+            g_time += time.perf_counter() - t
+        q_elems += xr.size + wr.size + dyr.size + wc.size + dyc.size + xc.size
         g_macs += tile * tile * (K + N + M)
     est = full_q * (q_time / q_elems) + full_macs * (g_time / g_macs)
     return {"tflops": 2 * full_macs / est / 1e12, "sample_seconds": q_time + g_time, "step_seconds": est}
 
 
-def cpu_baseline(lins, tile=64):
+def cpu_baseline(lins, tile=64, variant="fp32-scale"):
     import oracle
-    r = oracle_sample(host_slices(lins, tile), tile)
+    r = oracle_sample(host_slices(lins, tile), tile, variant)
     return {"value": r["tflops"], "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
             "sample": (f"per linear one {tile}x{tile} output block of Fprop, Dgrad and Wgrad plus the "
                        f"quantization of the operand slices it needs ({r['sample_seconds']:.1f} s of CPU "
@@ -506,16 +561,19 @@ def run_reference(args):
     lins = make_inputs(args.workload, device, args.tokens)
     sl = host_slices(lins, tile)
     del lins
-    vals = [oracle_sample(sl, tile) for _ in range(args.warmup + args.steps)][args.warmup:]
+    vals = [oracle_sample(sl, tile, args.variant) for _ in range(args.warmup + args.steps)][args.warmup:]
     value = statistics.median(v["tflops"] for v in vals)
     est = statistics.median(v["step_seconds"] for v in vals)
     cfg = workload_config(args.workload, args.tokens)
+    cfg["variant"] = VARIANTS[args.variant]
     cfg["parallelism"] = "host cores (oracle)"
     sample = (f"each step: per linear one {tile}x{tile} output block of Fprop, Dgrad and Wgrad plus the "
               f"quantization of the operand slices it needs; time extrapolated to the full step")
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": est * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64 oracle (E4M3 codes, FP32 scales)",
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": ("f64 oracle (E4M3 codes, E8M0 block exponents)" if args.variant == "mx"
+                      else "f64 oracle (E4M3 codes, FP32 scales)"),
             "data": "synthetic", "config": cfg,
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
                              "sample": sample},

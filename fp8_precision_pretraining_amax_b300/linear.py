@@ -70,6 +70,60 @@ class LinearFP8:
     LAUNCHES_PER_STEP = 6
 
 
+class LinearMX:
+    """The same linear layer on the MX variant: E4M3 codes with one
+    power-of-two scale per 1x32 block along each GEMM's reduction dimension,
+    applied by the tensor cores inside the MMA.  Every operand is quantized
+    along the dimension its GEMM reduces over, so W and X are each quantized
+    twice (row-wise for Fprop / column-wise for Dgrad and Wgrad) and so is dY.
+
+      forward    W -> row-wise (Fprop) and column-wise (Dgrad) codes
+                 X -> row-wise (Fprop) and column-wise (Wgrad) codes
+                 Y  = MX GEMM(Xq, Wq)                                   [M, N]
+      backward   dY -> row-wise (Dgrad) and column-wise (Wgrad) codes
+                 dX = MX GEMM(dYq, Wq^T)                                [M, K]
+                 dW = MX GEMM(dYq^T, Xq^T)                              [N, K]
+    """
+
+    def __init__(self, M: int, K: int, N: int, device="cuda"):
+        self.M, self.K, self.N = M, K, N
+        u8, bf = torch.uint8, torch.bfloat16
+        e = lambda *shape, dt=u8: torch.empty(shape, dtype=dt, device=device)
+        self.xq, self.ex = e(M, K), e(K // 128, M, 4)
+        self.xqT, self.exT = e(K, M), e(M // 128, K, 4)
+        self.wq, self.ew = e(N, K), e(K // 128, N, 4)
+        self.wqT, self.ewT = e(K, N), e(N // 128, K, 4)
+        self.dyq, self.edy = e(M, N), e(N // 128, M, 4)
+        self.dyqT, self.edyT = e(N, M), e(M // 128, N, 4)
+        self.y, self.dx, self.dw = e(M, N, dt=bf), e(M, K, dt=bf), e(N, K, dt=bf)
+
+    @property
+    def flops_per_gemm(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+    def forward(self, x: torch.Tensor, w: torch.Tensor) -> torch.Tensor:
+        fp8bq.fp8bq_mx_quantize_rowwise(w, self.wq, self.ew)
+        fp8bq.fp8bq_mx_quantize_colwise(w, self.wqT, self.ewT)
+        fp8bq.fp8bq_mx_quantize_rowwise(x, self.xq, self.ex)
+        fp8bq.fp8bq_mx_quantize_colwise(x, self.xqT, self.exT)
+        fp8bq.fp8bq_mx_gemm(self.xq, self.ex, self.wq, self.ew, self.y)
+        return self.y
+
+    def backward(self, dy: torch.Tensor):
+        fp8bq.fp8bq_mx_quantize_rowwise(dy, self.dyq, self.edy)
+        fp8bq.fp8bq_mx_quantize_colwise(dy, self.dyqT, self.edyT)
+        fp8bq.fp8bq_mx_gemm(self.dyq, self.edy, self.wqT, self.ewT, self.dx)
+        fp8bq.fp8bq_mx_gemm(self.dyqT, self.edyT, self.xqT, self.exT, self.dw)
+        return self.dx, self.dw
+
+    def step(self, x: torch.Tensor, w: torch.Tensor, dy: torch.Tensor):
+        self.forward(x, w)
+        self.backward(dy)
+        return self.y, self.dx, self.dw
+
+    LAUNCHES_PER_STEP = 9
+
+
 class SwiGLUMLPFP8:
     """Forward of a SwiGLU MLP (x -> gate/up -> silu(g) * u -> down) on the FP8
     path, with the SwiGLU gate fused into the down projection's quantizer.
