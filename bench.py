@@ -27,7 +27,7 @@ region), and the CPU oracle timed on a bounded sample on the host cores.
 
 --variant mx times the MX variant of the same step instead: every operand
 quantized with a power-of-two scale per 1x32 block along its GEMM's reduction
-dimension (row-wise and column-wise passes over X, W and dY) and the three
+dimension (one pass over each of X, W and dY emits both layouts) and the three
 GEMMs on the block-scaled MMA, which applies the scales itself.
 
 Multi-GPU (torchrun): data parallel with weak scaling.  Every rank runs the
@@ -245,18 +245,16 @@ def step_launches(fp8bq, L, lin):
 
 
 def step_launches_mx(fp8bq, L, lin):
-    """The MX variant's 9 launches per linear, in step order.  Quantizer bytes:
-    BF16 in, one code byte and 1/32 exponent byte per element and layout."""
+    """The MX variant's 6 launches per linear, in step order.  Quantizer bytes:
+    BF16 in once, one code byte and 1/32 exponent byte per element and layout."""
     M, K, N = L.M, L.K, L.N
-    one = lambda R, C: 2 * R * C + R * C + R * C // 32
+    both = lambda R, C: 2 * R * C + 2 * (R * C + R * C // 32)
     return [
-        ("quant_mx_rowwise", one(N, K), lambda: fp8bq.fp8bq_mx_quantize_rowwise(lin.w, L.wq, L.ew)),
-        ("quant_mx_colwise", one(N, K), lambda: fp8bq.fp8bq_mx_quantize_colwise(lin.w, L.wqT, L.ewT)),
-        ("quant_mx_rowwise", one(M, K), lambda: fp8bq.fp8bq_mx_quantize_rowwise(lin.x, L.xq, L.ex)),
-        ("quant_mx_colwise", one(M, K), lambda: fp8bq.fp8bq_mx_quantize_colwise(lin.x, L.xqT, L.exT)),
+        ("quant_mx_rowcol", both(N, K), lambda: fp8bq.fp8bq_mx_quantize_rowcol(lin.w, L.wq, L.ew, L.wqT, L.ewT)),
+        ("quant_mx_rowcol", both(M, K), lambda: fp8bq.fp8bq_mx_quantize_rowcol(lin.x, L.xq, L.ex, L.xqT, L.exT)),
         ("gemm_mx_fprop", 2 * M * N * K, lambda: fp8bq.fp8bq_mx_gemm(L.xq, L.ex, L.wq, L.ew, L.y)),
-        ("quant_mx_rowwise", one(M, N), lambda: fp8bq.fp8bq_mx_quantize_rowwise(lin.dy, L.dyq, L.edy)),
-        ("quant_mx_colwise", one(M, N), lambda: fp8bq.fp8bq_mx_quantize_colwise(lin.dy, L.dyqT, L.edyT)),
+        ("quant_mx_rowcol", both(M, N),
+         lambda: fp8bq.fp8bq_mx_quantize_rowcol(lin.dy, L.dyq, L.edy, L.dyqT, L.edyT)),
         ("gemm_mx_dgrad", 2 * M * N * K, lambda: fp8bq.fp8bq_mx_gemm(L.dyq, L.edy, L.wqT, L.ewT, L.dx)),
         ("gemm_mx_wgrad", 2 * M * N * K, lambda: fp8bq.fp8bq_mx_gemm(L.dyqT, L.edyT, L.xqT, L.exT, L.dw)),
     ]

@@ -98,7 +98,10 @@ int probe_device(DeviceState** out) {
             if (set_tile_smem<false>() != cudaSuccess || set_tile_smem<true>() != cudaSuccess) return FP8BQ_ERR_CUDA;
             if (cudaFuncSetAttribute(fp8bq::mx_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(fp8bq::kMxSmemBytes)) != cudaSuccess ||
-                cudaFuncSetAttribute(fp8bq::mx_quantize_colwise_kernel<true>,
+                cudaFuncSetAttribute(fp8bq::mx_quantize_slab_kernel<true, false>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     fp8bq::mx_col_smem_bytes<true>()) != cudaSuccess ||
+                cudaFuncSetAttribute(fp8bq::mx_quantize_slab_kernel<true, true>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      fp8bq::mx_col_smem_bytes<true>()) != cudaSuccess)
                 return FP8BQ_ERR_CUDA;
@@ -206,6 +209,23 @@ int encode_u8_out_map(CUtensorMap* map, void* ptr, uint64_t cols, uint64_t rows)
                                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? FP8BQ_OK : FP8BQ_ERR_CUDA;
+}
+
+// One 128x128 slab per CTA: grid (C/128, M/128).  Column-wise codes always,
+// row-wise codes too when kRows.
+template <bool kRows>
+int launch_mx_slab(const void* x, int dtype, int64_t M, int64_t C, int64_t ldx, uint8_t* qT, uint8_t* e8T,
+                   uint8_t* q, uint8_t* e8, cudaStream_t cs) {
+    dim3 grid(static_cast<unsigned>(C / 128), static_cast<unsigned>(M / 128));
+    uint16_t* ehT = reinterpret_cast<uint16_t*>(e8T);
+    uint16_t* eh = reinterpret_cast<uint16_t*>(e8);
+    if (dtype == FP8BQ_BF16)
+        fp8bq::mx_quantize_slab_kernel<false, kRows>
+            <<<grid, 256, fp8bq::mx_col_smem_bytes<false>(), cs>>>(x, M, C, ldx, qT, ehT, q, eh);
+    else
+        fp8bq::mx_quantize_slab_kernel<true, kRows>
+            <<<grid, 256, fp8bq::mx_col_smem_bytes<true>(), cs>>>(x, M, C, ldx, qT, ehT, q, eh);
+    return launch_status();
 }
 
 template <int MODE>
@@ -445,16 +465,24 @@ int fp8bq_mx_quantize_colwise(const void* x, int dtype, int64_t M, int64_t C, in
     DeviceState* dev = nullptr;
     int st = probe_device(&dev);
     if (st != FP8BQ_OK) return st;
-    dim3 grid(static_cast<unsigned>(C / 128), static_cast<unsigned>(M / 128));
-    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    uint16_t* eh = reinterpret_cast<uint16_t*>(e8);
-    if (dtype == FP8BQ_BF16)
-        fp8bq::mx_quantize_colwise_kernel<false>
-            <<<grid, 256, fp8bq::mx_col_smem_bytes<false>(), cs>>>(x, M, C, ldx, qT, eh);
-    else
-        fp8bq::mx_quantize_colwise_kernel<true>
-            <<<grid, 256, fp8bq::mx_col_smem_bytes<true>(), cs>>>(x, M, C, ldx, qT, eh);
-    return launch_status();
+    return launch_mx_slab<false>(x, dtype, M, C, ldx, qT, e8, nullptr, nullptr,
+                                 reinterpret_cast<cudaStream_t>(stream));
+}
+
+int fp8bq_mx_quantize_rowcol(const void* x, int dtype, int64_t M, int64_t C, int64_t ldx, uint8_t* q,
+                             uint8_t* e8, uint8_t* qT, uint8_t* e8T, fp8bq_stream_t stream) {
+    if (dtype != FP8BQ_BF16 && dtype != FP8BQ_F32) return FP8BQ_ERR_DTYPE;
+    if (M < 0 || C < 0 || ldx < C || (M % 128) || (C % 128)) return FP8BQ_ERR_SHAPE;
+    if (M == 0 || C == 0) return FP8BQ_OK;
+    if (!x || !q || !e8 || !qT || !e8T) return FP8BQ_ERR_NULL;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(e8) || !aligned16(qT) || !aligned16(e8T) ||
+        ((ldx * elem_size(dtype)) % 16))
+        return FP8BQ_ERR_ALIGN;
+    if (M / 128 > 65535 || C / 128 >= (int64_t(1) << 31)) return FP8BQ_ERR_SHAPE;
+    DeviceState* dev = nullptr;
+    int st = probe_device(&dev);
+    if (st != FP8BQ_OK) return st;
+    return launch_mx_slab<true>(x, dtype, M, C, ldx, qT, e8T, q, e8, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int fp8bq_mx_gemm(const uint8_t* a, const uint8_t* ea, const uint8_t* b, const uint8_t* eb, uint16_t* d, int64_t I,

@@ -17,7 +17,9 @@
 //
 // Kernels:
 //   mx_quantize_rowwise_kernel   streams 1x32 blocks with 16-byte loads
-//   mx_quantize_colwise_kernel   stages a 128x128 slab in shared memory
+//   mx_quantize_slab_kernel      stages a 128x128 slab in shared memory for
+//                                the column-wise layout, optionally also the
+//                                row-wise one from the same read
 //   mx_gemm_kernel               persistent, one CTA per SM, 128 x 192
 //                                output tiles, TMA ring, block-scaled MMA
 //                                accumulating the whole reduction in TMEM
@@ -138,22 +140,34 @@ __global__ void __launch_bounds__(256) mx_quantize_rowwise_kernel(const void* __
     }
 }
 
-// --------------------------------------------------------------- column-wise
+// ------------------------------------------------- column-wise (and row-wise)
 //
 // CTA = 256 threads, slab of 128 rows (m0..) x 128 columns (c0..), copied to
-// shared memory with 16-byte cp.async (row pitch 128 elements).  Thread t owns
-// column t & 127 and the 32-row blocks 2h, 2h + 1 (h = t >> 7): it reads its
-// 64 values down the column (a warp reads one contiguous row segment per
-// step: no bank conflicts), writes each block's 32 codes as two 16-byte
-// stores into the transposed output, and its two exponent bytes as one
-// 16-bit store.
+// shared memory with 16-byte cp.async (row pitch 128 elements), then read in
+// up to two ways:
+//   column view  thread t owns column t & 127 and the 32-row blocks 2h, 2h + 1
+//                (h = t >> 7): it reads its 64 values down the column (a warp
+//                reads one contiguous row segment per step: no bank
+//                conflicts), writes each block's 32 codes as two 16-byte
+//                stores into the transposed output qT [C][M] and its two
+//                exponent bytes as one 16-bit store.
+//   row view     (kRows) thread t owns row t >> 1 and the 64 columns of half
+//                t & 1 (two 1x32 blocks); it reads them as 16-byte chunks in
+//                the rotated order (i + lane) mod n, so the 8 lanes of a
+//                quarter-warp hit 8 different bank groups, keeps a per-block
+//                amax with predicated maxima and writes each chunk's codes to
+//                q [M][C] at the chunk's own position.
+// One read of x then serves both layouts: X (Fprop row-wise, Wgrad
+// column-wise), W (Fprop row-wise, Dgrad column-wise) and dY (Dgrad row-wise,
+// Wgrad column-wise).
 template <bool kF32>
 constexpr int mx_col_smem_bytes() { return 128 * 128 * (kF32 ? 4 : 2); }
 
-template <bool kF32>
-__global__ void __launch_bounds__(256) mx_quantize_colwise_kernel(const void* __restrict__ x, int64_t M, int64_t C,
-                                                                  int64_t ldx, uint8_t* __restrict__ qT,
-                                                                  uint16_t* __restrict__ eh) {
+template <bool kF32, bool kRows>
+__global__ void __launch_bounds__(256) mx_quantize_slab_kernel(const void* __restrict__ x, int64_t M, int64_t C,
+                                                               int64_t ldx, uint8_t* __restrict__ qT,
+                                                               uint16_t* __restrict__ ehT, uint8_t* __restrict__ q,
+                                                               uint16_t* __restrict__ eh) {
     extern __shared__ __align__(16) uint8_t slab[];
     constexpr int ES = kF32 ? 4 : 2;
     constexpr int CPR = 128 * ES / 16;  // 16-byte chunks per slab row
@@ -169,39 +183,86 @@ __global__ void __launch_bounds__(256) mx_quantize_colwise_kernel(const void* __
     cp_async_wait_all();
     __syncthreads();
 
-    const int c = threadIdx.x & 127;
-    const int h = threadIdx.x >> 7;
-    uint32_t bytes = 0;
+    {
+        const int c = threadIdx.x & 127;
+        const int h = threadIdx.x >> 7;
+        uint32_t bytes = 0;
 #pragma unroll
-    for (int bb = 0; bb < 2; ++bb) {
-        const int b = 2 * h + bb;
-        float v[32];
+        for (int bb = 0; bb < 2; ++bb) {
+            const int b = 2 * h + bb;
+            float v[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int row = 32 * b + i;
-            if (kF32)
-                v[i] = reinterpret_cast<const float*>(slab)[row * 128 + c];
-            else
-                v[i] = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(slab)[row * 128 + c])
-                                       << 16);
+            for (int i = 0; i < 32; ++i) {
+                const int row = 32 * b + i;
+                if (kF32)
+                    v[i] = reinterpret_cast<const float*>(slab)[row * 128 + c];
+                else
+                    v[i] = __uint_as_float(
+                        static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(slab)[row * 128 + c]) << 16);
+            }
+            float amax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+            const int e = mx_exponent(amax);
+            const float inv = mx_inv_scale(e);
+            uint8_t* dst = qT + (c0 + c) * M + m0 + 32 * b;
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const float* p = v + 16 * k;
+                *reinterpret_cast<uint4*>(dst + 16 * k) =
+                    make_uint4(mx_e4m3x4(p[0], p[1], p[2], p[3], inv), mx_e4m3x4(p[4], p[5], p[6], p[7], inv),
+                               mx_e4m3x4(p[8], p[9], p[10], p[11], inv), mx_e4m3x4(p[12], p[13], p[14], p[15], inv));
+            }
+            bytes |= static_cast<uint32_t>(e + 127) << (8 * bb);
         }
-        float amax = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-        const int e = mx_exponent(amax);
-        const float inv = mx_inv_scale(e);
-        uint8_t* dst = qT + (c0 + c) * M + m0 + 32 * b;
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const float* p = v + 16 * k;
-            *reinterpret_cast<uint4*>(dst + 16 * k) =
-                make_uint4(mx_e4m3x4(p[0], p[1], p[2], p[3], inv), mx_e4m3x4(p[4], p[5], p[6], p[7], inv),
-                           mx_e4m3x4(p[8], p[9], p[10], p[11], inv), mx_e4m3x4(p[12], p[13], p[14], p[15], inv));
-        }
-        bytes |= static_cast<uint32_t>(e + 127) << (8 * bb);
+        // bytes 2h, 2h + 1 of word (m0 / 128) * C + c0 + c
+        ehT[((m0 >> 7) * C + c0 + c) * 2 + h] = static_cast<uint16_t>(bytes);
     }
-    // bytes 2h, 2h + 1 of word (m0 / 128) * C + c0 + c
-    eh[((m0 >> 7) * C + c0 + c) * 2 + h] = static_cast<uint16_t>(bytes);
+
+    if (kRows) {
+        constexpr int NCH = 64 * ES / 16;     // 16-byte chunks in the thread's 64 columns (8 or 16)
+        constexpr int VPC = 16 / ES;          // values per chunk (8 or 4)
+        constexpr int CPB = NCH / 2;          // chunks per 32-element block
+        const int lane = threadIdx.x & 31;
+        const int r = threadIdx.x >> 1, hf = threadIdx.x & 1;
+        const uint8_t* rowp = slab + r * (128 * ES) + hf * (64 * ES);
+        uint4 w[NCH];
+#pragma unroll
+        for (int i = 0; i < NCH; ++i) w[i] = *reinterpret_cast<const uint4*>(rowp + 16 * ((i + lane) & (NCH - 1)));
+        float m[2] = {0.0f, 0.0f};
+#pragma unroll
+        for (int i = 0; i < NCH; ++i) {
+            float a;
+            if (!kF32)
+                a = bf16x2_max_halves(absmax_bf16x2(absmax_bf16x2(w[i].x, w[i].y), absmax_bf16x2(w[i].z, w[i].w)));
+            else
+                a = fmaxf(fmaxf(fabsf(__uint_as_float(w[i].x)), fabsf(__uint_as_float(w[i].y))),
+                          fmaxf(fabsf(__uint_as_float(w[i].z)), fabsf(__uint_as_float(w[i].w))));
+            const bool second = ((i + lane) & (NCH - 1)) >= CPB;
+            m[0] = second ? m[0] : fmaxf(m[0], a);
+            m[1] = second ? fmaxf(m[1], a) : m[1];
+        }
+        const int e0 = mx_exponent(m[0]), e1 = mx_exponent(m[1]);
+        const float inv0 = mx_inv_scale(e0), inv1 = mx_inv_scale(e1);
+        uint8_t* dst = q + (m0 + r) * C + c0 + hf * 64;
+#pragma unroll
+        for (int i = 0; i < NCH; ++i) {
+            const int ch = (i + lane) & (NCH - 1);
+            const float inv = ch >= CPB ? inv1 : inv0;
+            if (!kF32) {
+                float f[8];
+                unpack_bf16x8(w[i], f);
+                *reinterpret_cast<uint2*>(dst + 8 * ch) =
+                    make_uint2(mx_e4m3x4(f[0], f[1], f[2], f[3], inv), mx_e4m3x4(f[4], f[5], f[6], f[7], inv));
+            } else {
+                *reinterpret_cast<uint32_t*>(dst + 4 * ch) =
+                    mx_e4m3x4(__uint_as_float(w[i].x), __uint_as_float(w[i].y), __uint_as_float(w[i].z),
+                              __uint_as_float(w[i].w), inv);
+            }
+        }
+        // bytes 2hf, 2hf + 1 of word (c0 / 128) * M + m0 + r
+        eh[((c0 >> 7) * M + m0 + r) * 2 + hf] = static_cast<uint16_t>((e0 + 127) | ((e1 + 127) << 8));
+    }
 }
 
 // ---------------------------------------------------------------------- GEMM

@@ -28,7 +28,7 @@ C_FUNCTIONS = (
     "fp8bq_quantize_rowwise", "fp8bq_quantize_colwise", "fp8bq_quantize_rowcol", "fp8bq_swiglu_quantize",
     "fp8bq_quantize_weight_block", "fp8bq_gemm_fprop", "fp8bq_gemm_fprop_q", "fp8bq_gemm_dgrad",
     "fp8bq_gemm_wgrad", "fp8bq_gemm_wgrad_f32", "fp8bq_mx_quantize_rowwise", "fp8bq_mx_quantize_colwise",
-    "fp8bq_mx_gemm", "fp8bq_check", "fp8bq_status_string", "fp8bq_selftest_wait_timeout",
+    "fp8bq_mx_quantize_rowcol", "fp8bq_mx_gemm", "fp8bq_check", "fp8bq_status_string", "fp8bq_selftest_wait_timeout",
 )
 
 
@@ -52,6 +52,7 @@ def _load():
         "fp8bq_gemm_wgrad_f32": [vp, vp, vp, vp, vp, i64, i64, i64, i32, vp],
         "fp8bq_mx_quantize_rowwise": [vp, i32, i64, i64, i64, vp, vp, vp],
         "fp8bq_mx_quantize_colwise": [vp, i32, i64, i64, i64, vp, vp, vp],
+        "fp8bq_mx_quantize_rowcol": [vp, i32, i64, i64, i64, vp, vp, vp, vp, vp],
         "fp8bq_mx_gemm": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
         "fp8bq_check": [vp],
         "fp8bq_selftest_wait_timeout": [i64, vp],
@@ -292,6 +293,20 @@ def fp8bq_mx_quantize_colwise(x: torch.Tensor, qT: torch.Tensor, e8: torch.Tenso
                "fp8bq_mx_quantize_colwise")
 
 
+def fp8bq_mx_quantize_rowcol(x: torch.Tensor, q: torch.Tensor, e8: torch.Tensor, qT: torch.Tensor,
+                             e8T: torch.Tensor) -> None:
+    """MX variant, both layouts from one read: x [M, C] -> q [M, C], e8 [C/128, M, 4], qT [C, M], e8T [M/128, C, 4]."""
+    ldx = _rows_input(x, "x")
+    M, C = x.shape
+    _need(q, torch.uint8, (M, C), "q")
+    _need(e8, torch.uint8, (C // 128, M, 4), "e8")
+    _need(qT, torch.uint8, (C, M), "qT")
+    _need(e8T, torch.uint8, (M // 128, C, 4), "e8T")
+    with torch.cuda.device(x.device):
+        _raise(lib.fp8bq_mx_quantize_rowcol(_ptr(x), _dtype_code(x), M, C, ldx, _ptr(q), _ptr(e8), _ptr(qT),
+                                            _ptr(e8T), _stream(x)), "fp8bq_mx_quantize_rowcol")
+
+
 def fp8bq_mx_gemm(a, ea, b, eb, d) -> None:
     """MX variant.  d [I, J] bf16 = (2^ea a)(2^eb b)^T: a [I, K], ea [K/128, I, 4], b [J, K], eb [K/128, J, 4]."""
     I, K = a.shape
@@ -427,6 +442,17 @@ def mx_quantize_colwise(x: torch.Tensor) -> Tuple[torch.Tensor, torch.Tensor]:
     e8 = torch.empty((M // 128, C, 4), dtype=torch.uint8, device=x.device)
     fp8bq_mx_quantize_colwise(x, qT, e8)
     return qT, e8
+
+
+def mx_quantize_rowcol(x: torch.Tensor):
+    """MX variant: returns (q, e8, qT, e8T)."""
+    M, C = x.shape
+    q = torch.empty((M, C), dtype=torch.uint8, device=x.device)
+    e8 = torch.empty((C // 128, M, 4), dtype=torch.uint8, device=x.device)
+    qT = torch.empty((C, M), dtype=torch.uint8, device=x.device)
+    e8T = torch.empty((M // 128, C, 4), dtype=torch.uint8, device=x.device)
+    fp8bq_mx_quantize_rowcol(x, q, e8, qT, e8T)
+    return q, e8, qT, e8T
 
 
 def mx_gemm(a, ea, b, eb) -> torch.Tensor:

@@ -74,13 +74,13 @@ class LinearMX:
     """The same linear layer on the MX variant: E4M3 codes with one
     power-of-two scale per 1x32 block along each GEMM's reduction dimension,
     applied by the tensor cores inside the MMA.  Every operand is quantized
-    along the dimension its GEMM reduces over, so W and X are each quantized
-    twice (row-wise for Fprop / column-wise for Dgrad and Wgrad) and so is dY.
+    along the dimension its GEMM reduces over, so X, W and dY each need both
+    layouts; one pass over each tensor produces them.
 
-      forward    W -> row-wise (Fprop) and column-wise (Dgrad) codes
-                 X -> row-wise (Fprop) and column-wise (Wgrad) codes
+      forward    W -> row-wise (Fprop) and column-wise (Dgrad) codes, one pass
+                 X -> row-wise (Fprop) and column-wise (Wgrad) codes, one pass
                  Y  = MX GEMM(Xq, Wq)                                   [M, N]
-      backward   dY -> row-wise (Dgrad) and column-wise (Wgrad) codes
+      backward   dY -> row-wise (Dgrad) and column-wise (Wgrad) codes, one pass
                  dX = MX GEMM(dYq, Wq^T)                                [M, K]
                  dW = MX GEMM(dYq^T, Xq^T)                              [N, K]
     """
@@ -102,16 +102,13 @@ class LinearMX:
         return 2 * self.M * self.N * self.K
 
     def forward(self, x: torch.Tensor, w: torch.Tensor) -> torch.Tensor:
-        fp8bq.fp8bq_mx_quantize_rowwise(w, self.wq, self.ew)
-        fp8bq.fp8bq_mx_quantize_colwise(w, self.wqT, self.ewT)
-        fp8bq.fp8bq_mx_quantize_rowwise(x, self.xq, self.ex)
-        fp8bq.fp8bq_mx_quantize_colwise(x, self.xqT, self.exT)
+        fp8bq.fp8bq_mx_quantize_rowcol(w, self.wq, self.ew, self.wqT, self.ewT)
+        fp8bq.fp8bq_mx_quantize_rowcol(x, self.xq, self.ex, self.xqT, self.exT)
         fp8bq.fp8bq_mx_gemm(self.xq, self.ex, self.wq, self.ew, self.y)
         return self.y
 
     def backward(self, dy: torch.Tensor):
-        fp8bq.fp8bq_mx_quantize_rowwise(dy, self.dyq, self.edy)
-        fp8bq.fp8bq_mx_quantize_colwise(dy, self.dyqT, self.edyT)
+        fp8bq.fp8bq_mx_quantize_rowcol(dy, self.dyq, self.edy, self.dyqT, self.edyT)
         fp8bq.fp8bq_mx_gemm(self.dyq, self.edy, self.wqT, self.ewT, self.dx)
         fp8bq.fp8bq_mx_gemm(self.dyqT, self.edyT, self.xqT, self.exT, self.dw)
         return self.dx, self.dw
@@ -121,7 +118,7 @@ class LinearMX:
         self.backward(dy)
         return self.y, self.dx, self.dw
 
-    LAUNCHES_PER_STEP = 9
+    LAUNCHES_PER_STEP = 6
 
 
 class SwiGLUMLPFP8:

@@ -247,6 +247,19 @@ int fp8bq_mx_quantize_colwise(const void* x, int dtype, int64_t M, int64_t C, in
                               uint8_t* e8, fp8bq_stream_t stream);
 
 /*
+ * Row-wise and column-wise MX quantization from one read of x: the outputs
+ * of fp8bq_mx_quantize_rowwise (q, e8) and fp8bq_mx_quantize_colwise
+ * (qT, e8T), bit for bit.
+ *   x    [M][C] BF16 or FP32, row pitch ldx elements (ldx >= C)
+ *   q    [M][C] codes,   e8  [C/128][M][4] exponents (1x32 blocks along C)
+ *   qT   [C][M] codes,   e8T [M/128][C][4] exponents (32x1 blocks along M)
+ * Requires M % 128 == 0, C % 128 == 0, M / 128 <= 65535.  One pass serves
+ * X (Fprop and Wgrad), W (Fprop and Dgrad) and dY (Dgrad and Wgrad).
+ */
+int fp8bq_mx_quantize_rowcol(const void* x, int dtype, int64_t M, int64_t C, int64_t ldx, uint8_t* q,
+                             uint8_t* e8, uint8_t* qT, uint8_t* e8T, fp8bq_stream_t stream);
+
+/*
  * MX GEMM: d[i][j] = BF16( sum_k 2^(ea(i,k)-127) D(a[i][k]) * 2^(eb(j,k)-127) D(b[j][k]) )
  * for two K-major operands as the MX quantizers emit them:
  *   a   [I][K] codes, ea [K/128][I][4] exponents

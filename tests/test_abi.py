@@ -150,6 +150,14 @@ def test_mx_entry_points_reject_bad_arguments_on_the_host(lib):
         assert f(P, 1, 128, 128, 130, P, P, None) == ERR_ALIGN       # 520-byte pitch
     g = lib.fp8bq_mx_quantize_colwise
     assert g(P, 0, 96, 128, 128, P, P, None) == ERR_SHAPE            # M not a multiple of 128
+    rc = lib.fp8bq_mx_quantize_rowcol
+    rc.restype, rc.argtypes = i32, [vp, i32, i64, i64, i64, vp, vp, vp, vp, vp]
+    assert rc(P, 0, 128, 200, 200, P, P, P, P, None) == ERR_SHAPE
+    assert rc(P, 0, 96, 128, 128, P, P, P, P, None) == ERR_SHAPE
+    assert rc(P, 0, 128, 128, 128, P, P, None, P, None) == ERR_NULL
+    assert rc(P, 0, 128, 128, 128, P, P, P, P + 2, None) == ERR_ALIGN
+    assert rc(P, 9, 128, 128, 128, P, P, P, P, None) == ERR_DTYPE
+    assert rc(P, 0, 0, 128, 128, None, None, None, None, None) == OK
     m = lib.fp8bq_mx_gemm
     m.restype, m.argtypes = i32, [vp] * 5 + [i64] * 3 + [vp]
     assert m(P, P, P, P, P, 128, 128, 100, None) == ERR_SHAPE

@@ -88,6 +88,38 @@ def test_mx_colwise_fp32_and_pitch(fb):
     _colwise_case(fb, xt[:, 128:384])
 
 
+def _rowcol_case(fb, x):
+    q, e8, qT, e8T = fb.mx_quantize_rowcol(x)
+    fb.check()
+    h = host_input(x)
+    wq, we = oracle.mx_quantize_rowwise(h)
+    wqT, weT = oracle.mx_quantize_colwise(h)
+    assert_codes_equal(q.cpu().numpy(), wq, "mx rowcol row-wise codes")
+    assert_codes_equal(e8.cpu().numpy(), we, "mx rowcol row-wise exponents")
+    assert_codes_equal(qT.cpu().numpy(), wqT, "mx rowcol column-wise codes")
+    assert_codes_equal(e8T.cpu().numpy(), weT, "mx rowcol column-wise exponents")
+
+
+@pytest.mark.parametrize("M,C", [(128, 128), (384, 256), (256, 640)])
+def test_mx_rowcol_bf16(fb, M, C):
+    gen = synth.generator(300 + M + C)
+    x = synth.activations(M, C, gen).cuda()
+    x[5, 32:64] = 0.0
+    x[64:96, 7] = 0.0
+    x[-1, :] *= 2.0 ** -118
+    _rowcol_case(fb, x)
+
+
+def test_mx_rowcol_fp32_and_pitch(fb):
+    rng = np.random.default_rng(9)
+    x = (rng.standard_normal((256, 640)) * np.exp2(rng.integers(-50, 50, (256, 1)))).astype(np.float32)
+    xt = torch.from_numpy(x).cuda()
+    _rowcol_case(fb, xt)
+    _rowcol_case(fb, xt[:, 128:512])
+    gen = synth.generator(10)
+    _rowcol_case(fb, synth.activations(128, 768, gen).cuda()[:, 256:640])
+
+
 def _rand_exps(rng, shape, lo=112, hi=136):
     return rng.integers(lo, hi + 1, size=shape).astype(np.uint8)
 
@@ -160,23 +192,19 @@ def test_mx_gemm_empty_reduction_writes_zeros(fb):
 
 
 def test_mx_linear_layer_fprop_dgrad_wgrad(fb):
-    """The three products of one linear layer from the MX quantizers, end to
-    end on the GPU, against the oracle applied to the same codes."""
+    """One step of LinearMX (three row+column quantizer passes, three MX
+    GEMMs) on the GPU, against the oracle's quantizers and GEMM."""
     gen = synth.generator(43)
     M, K, N = 512, 384, 640
     x = synth.activations(M, K, gen).cuda()
     w = synth.weight(N, K, gen).cuda()
     dy = synth.grads(M, N, gen).cuda()
-    xq, ex = fb.mx_quantize_rowwise(x)
-    wq, ew = fb.mx_quantize_rowwise(w)
-    dyq, edy = fb.mx_quantize_rowwise(dy)
-    wqT, ewT = fb.mx_quantize_colwise(w)
-    dyqT, edyT = fb.mx_quantize_colwise(dy)
-    xqT, exT = fb.mx_quantize_colwise(x)
-    y = fb.mx_gemm(xq, ex, wq, ew)
-    dx = fb.mx_gemm(dyq, edy, wqT, ewT)
-    dw = fb.mx_gemm(dyqT, edyT, xqT, exT)
+    from fp8_precision_pretraining_amax_b300.linear import LinearMX
+    L = LinearMX(M, K, N, device="cuda")
+    y, dx, dw = L.step(x, w, dy)
     fb.check()
+    xq, ex, wq, ew, dyq, edy = L.xq, L.ex, L.wq, L.ew, L.dyq, L.edy
+    wqT, ewT, dyqT, edyT, xqT, exT = L.wqT, L.ewT, L.dyqT, L.edyT, L.xqT, L.exT
     # every quantizer output equals the oracle's; the GEMM checks then take
     # the oracle's codes as their inputs
     want = {}
