@@ -221,7 +221,6 @@ __global__ void __launch_bounds__(256) mx_quantize_slab_kernel(const void* __res
 
     if (kRows) {
         constexpr int NCH = 64 * ES / 16;     // 16-byte chunks in the thread's 64 columns (8 or 16)
-        constexpr int VPC = 16 / ES;          // values per chunk (8 or 4)
         constexpr int CPB = NCH / 2;          // chunks per 32-element block
         const int lane = threadIdx.x & 31;
         const int r = threadIdx.x >> 1, hf = threadIdx.x & 1;
