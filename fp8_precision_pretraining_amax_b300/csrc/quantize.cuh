@@ -41,65 +41,67 @@ __device__ __forceinline__ float tile_scale(float amax) {
 // exhaustively over every pair of BF16 values (x, amax), |x| <= amax.
 constexpr float kRecipMinAmax = 0x1p-80f;
 
-// Per-tile divisor: the scale, its negation and its correctly rounded
-// reciprocal.  r == 0 marks a tile that needs IEEE division (amax < 2^-80);
-// this lets the divisor travel through shared memory as two floats.
+// Per-tile divisor: the scale, its negation and the negated correctly
+// rounded reciprocal -RN(1/s).  nr == 0 marks a tile that needs IEEE division
+// (amax < 2^-80); this lets the divisor travel through shared memory as two
+// floats (s, nr).
 struct TileDiv {
-    float s, ns, r;
+    float s, ns, nr;
 };
 
 __device__ __forceinline__ TileDiv tile_div(float amax) {
     TileDiv d;
     d.s = tile_scale(amax);
     d.ns = -d.s;
-    d.r = amax >= kRecipMinAmax ? __frcp_rn(d.s) : 0.0f;
+    d.nr = amax >= kRecipMinAmax ? -__frcp_rn(d.s) : 0.0f;
     return d;
 }
 
-__device__ __forceinline__ TileDiv tile_div_from(float s, float r) {
+__device__ __forceinline__ TileDiv tile_div_from(float s, float nr) {
     TileDiv d;
     d.s = s;
     d.ns = -s;
-    d.r = r;
+    d.nr = nr;
     return d;
 }
 
-__device__ __forceinline__ bool tile_fast(const TileDiv& d) { return d.r != 0.0f; }
+__device__ __forceinline__ bool tile_fast(const TileDiv& d) { return d.nr != 0.0f; }
 
-// Sign of x copied onto q: x / s carries the sign of x (s > 0), which the
-// correction step below loses for x = -0 only.
-__device__ __forceinline__ float with_sign_of(float q, float x) {
-    return __uint_as_float(__float_as_uint(q) | (__float_as_uint(x) & 0x80000000u));
-}
-
-// Two correctly rounded quotients a / s, b / s.  Fast path (Markstein's
-// division theorem, "Computation of elementary functions on the IBM RISC
-// System/6000 processor", IBM J. Res. Dev. 34(1), 1990): with r = RN(1/s),
-// q0 = RN(x r) lies within one ulp of x / s, the residual x - q0 s is exact
-// under FMA, and q0 + r (x - q0 s) rounded once is RN(x / s).  Packed f32x2
-// arithmetic, two quotients per instruction.  The slow path (tiny tiles) is
-// IEEE division.  Callers choose the path once per tile.
+// Two NEGATED correctly rounded quotients -RN(a / s), -RN(b / s).  Fast path
+// (Markstein's division theorem, "Computation of elementary functions on the
+// IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990): with
+// r = RN(1/s), q0 = RN(x r) lies within one ulp of x / s, the residual
+// x - q0 s is exact under FMA, and q0 + r (x - q0 s) rounded once is
+// RN(x / s).  It runs on the negated quantities q0' = RN(x (-r)) = -q0 and
+// e = x + q0' s, giving RN(q0' - e r) = -RN(x / s); rounding to nearest is
+// symmetric, so only signed zeros could differ, and those come out negated
+// too (x = -0 gives +0, x = +0 gives -0), so the sign flip after the E4M3
+// conversion restores every code.  Packed f32x2 arithmetic, two quotients per
+// instruction.  The slow path (tiny tiles) is IEEE division by -s.  Callers
+// choose the path once per tile.
 template <bool kFast>
-__device__ __forceinline__ float2 quot2(float a, float b, const TileDiv& d) {
-    if (!kFast) return make_float2(__fdiv_rn(a, d.s), __fdiv_rn(b, d.s));
+__device__ __forceinline__ float2 neg_quot2(float a, float b, const TileDiv& d) {
+    if (!kFast) return make_float2(__fdiv_rn(a, d.ns), __fdiv_rn(b, d.ns));
     float q0a, q0b;
-    fmul2(q0a, q0b, a, b, d.r, d.r);
+    fmul2(q0a, q0b, a, b, d.nr, d.nr);    // q0' = -RN(x r)
     float ea = a, eb = b;
-    ffma2(ea, eb, q0a, q0b, d.ns, d.ns);  // e = x - q0 s (exact)
-    ffma2(q0a, q0b, ea, eb, d.r, d.r);    // q = q0 + e r
-    return make_float2(with_sign_of(q0a, a), with_sign_of(q0b, b));
+    ffma2(ea, eb, q0a, q0b, d.s, d.s);    // e = x - RN(x r) s (exact)
+    ffma2(q0a, q0b, ea, eb, d.nr, d.nr);  // q0' - e r = -(q0 + e r)
+    return make_float2(q0a, q0b);
 }
 
-// Two values -> two E4M3 codes packed low byte first (element a first).
+// Two values -> the E4M3 codes of their negated quotients, packed low byte
+// first (element a first).  E4M3 with saturation is symmetric in the sign.
 template <bool kFast>
-__device__ __forceinline__ uint32_t e4m3x2(float a, float b, const TileDiv& d) {
-    return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(quot2<kFast>(a, b, d), __NV_SATFINITE, __NV_E4M3));
+__device__ __forceinline__ uint32_t neg_e4m3x2(float a, float b, const TileDiv& d) {
+    return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(neg_quot2<kFast>(a, b, d), __NV_SATFINITE, __NV_E4M3));
 }
 
-// Four values -> four codes in one 32-bit word (memory order).
+// Four values -> four codes of x / s in one 32-bit word (memory order): the
+// codes of -x / s with every sign bit flipped.
 template <bool kFast>
 __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float e, const TileDiv& d) {
-    return e4m3x2<kFast>(a, b, d) | (e4m3x2<kFast>(c, e, d) << 16);
+    return (neg_e4m3x2<kFast>(a, b, d) | (neg_e4m3x2<kFast>(c, e, d) << 16)) ^ 0x80808080u;
 }
 
 // Eight values -> eight codes (memory order), path chosen per tile.
@@ -305,7 +307,7 @@ __global__ void __launch_bounds__(256, 4) quantize_tile_kernel(const void* __res
     constexpr int RPG = 128 / G;      // rows per group
     extern __shared__ __align__(16) uint8_t slab[];
     __shared__ float red[G][128];
-    __shared__ float cdiv[2][128];    // per column (or [.][0] for the block): s, r
+    __shared__ float cdiv[2][128];    // per column (or [.][0] for the block): s, nr
     __shared__ float wred[8];
 
     const int tid = threadIdx.x;
@@ -388,7 +390,7 @@ __global__ void __launch_bounds__(256, 4) quantize_tile_kernel(const void* __res
             for (int gg = 1; gg < G; ++gg) a = fmaxf(a, red[gg][tid]);
             const TileDiv d = tile_div(a);
             cdiv[0][tid] = d.s;
-            cdiv[1][tid] = d.r;
+            cdiv[1][tid] = d.nr;
             if (c0 + tid < C) s_col[(r0 >> 7) * C + c0 + tid] = d.s;
         }
     } else {
@@ -405,7 +407,7 @@ __global__ void __launch_bounds__(256, 4) quantize_tile_kernel(const void* __res
             for (int w = 1; w < 8; ++w) a = fmaxf(a, wred[w]);
             const TileDiv d = tile_div(a);
             cdiv[0][0] = d.s;
-            cdiv[1][0] = d.r;
+            cdiv[1][0] = d.nr;
             s_row[(r0 >> 7) * (C >> 7) + (c0 >> 7)] = d.s;
         }
     }
