@@ -1,0 +1,71 @@
+"""Host-side pieces of bench.py: workload bookkeeping, the launch plans, the
+committed ncu traffic records, and the reference arm (the oracle on the host
+cores), which runs without a GPU."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def test_layer_workload_shapes_and_flops():
+    shapes = bench.workload_shapes("layer_3p8b")
+    assert [(n, M, K, N) for n, M, K, N in shapes] == [
+        ("qkv", 32768, 3072, 4608), ("o", 32768, 3072, 3072), ("gate_up", 32768, 3072, 16384),
+        ("down", 32768, 8192, 3072)]
+    # Fprop, Dgrad and Wgrad of every linear, 2 M N K each
+    assert bench.step_flops(shapes) == sum(3 * 2 * M * N * K for _, M, K, N in shapes)
+    assert abs(bench.step_flops(shapes) / 1e12 - 19.48) < 0.01
+    assert bench.workload_shapes("layer_3p8b", tokens=8192)[0][1] == 8192
+
+
+class _Layer:
+    def __init__(self, M, K, N):
+        self.M, self.K, self.N = M, K, N
+
+
+def test_launch_plans_count_the_work_once():
+    from fp8_precision_pretraining_amax_b300 import fp8bq  # loads the library; no CUDA call
+    M, K, N = 256, 384, 640
+    L, lin = _Layer(M, K, N), None
+    plan = bench.step_launches(fp8bq, L, lin)
+    kinds = [k for k, _, _ in plan]
+    assert kinds == ["quant_weight", "quant_rowcol", "gemm_fprop", "quant_rowcol", "gemm_dgrad", "gemm_wgrad"]
+    assert sum(w for k, w, _ in plan if k.startswith("gemm")) == 3 * 2 * M * N * K
+    mx = bench.step_launches_mx(fp8bq, L, lin)
+    assert [k for k, _, _ in mx] == ["quant_mx_rowcol", "quant_mx_rowcol", "gemm_mx_fprop", "quant_mx_rowcol",
+                                    "gemm_mx_dgrad", "gemm_mx_wgrad"]
+    # one BF16 read, two code layouts, one exponent byte per 32 codes of each layout
+    assert mx[0][1] == 2 * N * K + 2 * (N * K + N * K // 32)
+
+
+@pytest.mark.parametrize("variant,src", [("fp32-scale", "gemm.cuh"), ("mx", "mx.cuh")])
+def test_committed_traffic_records(variant, src):
+    """A record is used only while its sha256 matches the kernel source; a
+    stale one makes bench.py report traffic as null (not a wrong number)."""
+    rec = bench.gemm_traffic_record(variant)
+    if rec is None:
+        pytest.skip(f"the DRAM record for {src} predates the current source: bench.py reports null")
+    assert rec["workload"] == "layer_3p8b"
+    assert float(rec["dram_bytes_per_launch"]) > float(rec["algorithmic_bytes_per_launch"]) > 0
+
+
+@pytest.mark.parametrize("variant", ["fp32-scale", "mx"])
+def test_reference_arm_prints_one_json_line(variant):
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                          "tiny", "--steps", "1", "--warmup", "1", "--variant", variant],
+                         capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "TFLOP/s"
+    assert d["value"] > 0 and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["config"]["workload"] == "tiny" and d["config"]["variant"] == bench.VARIANTS[variant]
