@@ -260,3 +260,26 @@ def test_accuracy_against_the_fp32_scale_layer_on_outlier_activations():
     e_bs, e_mx = rel(y_fp32_scale), rel(y_mx)
     print(f"relative error: FP32-scale 1x128/128x128 {e_bs:.4f}, MX 1x32 power-of-two {e_mx:.4f}")
     assert 0 < e_bs < 2 * 2.0 ** -4 and 0 < e_mx < 2 * 2.0 ** -4
+
+
+def test_accuracy_against_the_fp32_scale_layer_on_gradients():
+    """The same comparison for a Dgrad-shaped product of N(0,1e-3) output
+    gradients (no outliers) with N(0,0.02) weights: dX = dY W, dY row-wise
+    along N, W column-wise (MX) or in 128x128 blocks (FP32-scale layer).
+    Measured about 3.7 % (FP32-scale) and 3.8 % (MX) with these seeds."""
+    gen = synth.generator(3)
+    M, N, K = 512, 2048, 256
+    dy = synth.grads(M, N, gen)
+    w = synth.weight(N, K, gen)
+    dyb, wb = synth.bf16_bits(dy), synth.bf16_bits(w)
+    exact = dy.double().numpy() @ w.double().numpy()
+    dyq, sdy = oracle.quantize_rowwise(dyb)
+    wq, _, sw = oracle.quantize_weight_block(wb)
+    dx_fp32_scale, _ = oracle.gemm_dgrad(dyq, sdy, wq, sw)
+    dym, edy = oracle.mx_quantize_rowwise(dyb)
+    wmT, ewT = oracle.mx_quantize_colwise(wb)
+    dx_mx, _ = oracle.mx_gemm(dym, edy, wmT, ewT)
+    rel = lambda y: float(np.linalg.norm(y - exact) / np.linalg.norm(exact))
+    e_bs, e_mx = rel(dx_fp32_scale), rel(dx_mx)
+    print(f"relative error (Dgrad): FP32-scale {e_bs:.4f}, MX {e_mx:.4f}")
+    assert 0 < e_bs < 2 * 2.0 ** -4 and 0 < e_mx < 2 * 2.0 ** -4
