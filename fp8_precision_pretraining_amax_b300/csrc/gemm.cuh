@@ -119,6 +119,7 @@ struct alignas(16) GemmCtl {
     int abort;
     uint32_t issued;           // loads this CTA's producer issued
     uint32_t peer_issued;      // even CTA: loads the odd CTA's producer issued
+    uint32_t scl_issued;       // scale slots this CTA's scale producer filled
     ScaleSlot scl[kScaleSlots];
 };
 static_assert(offsetof(GemmCtl, scl) % 16 == 0, "scale slots are read with 16-byte vector loads");
@@ -214,6 +215,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         ctl->abort = 0;
         ctl->issued = 0;
         ctl->peer_issued = 0;
+        ctl->scl_issued = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
@@ -269,7 +271,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // completion in bytes), Fprop/Dgrad's weight-block scale of each
         // 128-column half with two 4-byte cp.async.  Rows and columns past
         // the problem are skipped.
-        uint32_t q = 0, qph = 0;
+        uint32_t q = 0, qph = 0, issued = 0;
         bool ok = true;
         for (int tile = first_tile; tile < p.num_tiles && ok; tile += tile_step) {
             const int tm = tile / p.tiles_n, tn = tile - tm * p.tiles_n;
@@ -295,11 +297,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                     cp_async_arrive(&ctl->sfull[q]);
                 }
+                ++issued;
                 if (++q == kScaleSlots) { q = 0; qph ^= 1; }
             }
         }
         cp_async_drain();
         if (!ok) raise_abort(ctl, peer_abort, status);
+        if (lane == 0) ctl->scl_issued = issued;
     } else if (warp == 1 && leader) {
         // --------------------------------------------------------------- MMA
         // One thread runs the whole loop (no per-wait warp broadcast).
@@ -541,14 +545,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
 
     // Teardown.  Every role has stopped (all waits are bounded).  The odd CTA
-    // reports how many loads its producer issued; after an abort the even CTA
-    // waits (bounded) for every copy either producer issued and for its own
-    // in-flight MMAs, which read both CTAs' shared memory and write both
-    // CTAs' TMEM, before either CTA frees TMEM or exits.
+    // reports how many loads its producer issued; after an abort each CTA
+    // waits (bounded) for the scale copies it issued, and the even CTA for
+    // every operand copy either producer issued and for its own in-flight
+    // MMAs, which read both CTAs' shared memory and write both CTAs' TMEM,
+    // before either CTA frees TMEM or exits.  Only the last ring-depth copies
+    // can still be in flight: a slot is refilled only after its previous
+    // contents were consumed.
     tc_fence_before();
     __syncthreads();
     if (!leader && threadIdx.x == 0) st_cluster_u32(mapa_shared(smem_addr(&ctl->peer_issued), 0), ctl->issued);
     cluster_sync_all();
+    if (*abort_flag && warp == 2 && lane == 0) {
+        const uint32_t n = ctl->scl_issued;
+        const uint32_t f0 = n > static_cast<uint32_t>(kScaleSlots) ? n - kScaleSlots : 0;
+        for (uint32_t f = f0; f < n; ++f)
+            bounded_wait(&ctl->sfull[f % kScaleSlots], (f / kScaleSlots) & 1, nullptr, lim);
+    }
     if (leader && *abort_flag) {
         if (warp == 0 && lane == 0) {
             const uint32_t n = ctl->issued > ctl->peer_issued ? ctl->issued : ctl->peer_issued;
