@@ -70,34 +70,6 @@ __device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, vol
     }
 }
 
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return done != 0;
-}
-
-// bounded_wait for a single thread that has nothing else to do: polls
-// without suspending, so it resumes as soon as the phase completes.
-__device__ __forceinline__ bool bounded_spin(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                             uint64_t limit_ns) {
-    const uint32_t a = smem_addr(bar);
-    if (mbar_test_wait(a, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
-#pragma unroll 1
-        for (int i = 0; i < 64; ++i)
-            if (mbar_test_wait(a, parity)) return true;
-        if (abort_flag != nullptr && *abort_flag) return false;
-        if (globaltimer_ns() - t0 > limit_ns) return false;
-    }
-}
-
 // bounded_wait for a thread that is usually far ahead of its consumers (the
 // copy producers): between polls it sleeps `sleep_ns`, so the warps it shares
 // an SM sub-partition with keep its issue slots.
@@ -218,17 +190,6 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
     return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, one M x N x 32 step (single CTA).
-__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                         uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -332,11 +293,6 @@ __device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, 
         "mov.b64 {%0, %1}, rd;\n\t}"
         : "=f"(d0), "=f"(d1)
         : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
-}
-
-// Named barrier among `nthreads` threads (a multiple of 32) of the CTA.
-__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 }  // namespace fp8bq
