@@ -283,3 +283,21 @@ def test_accuracy_against_the_fp32_scale_layer_on_gradients():
     e_bs, e_mx = rel(dx_fp32_scale), rel(dx_mx)
     print(f"relative error (Dgrad): FP32-scale {e_bs:.4f}, MX {e_mx:.4f}")
     assert 0 < e_bs < 2 * 2.0 ** -4 and 0 < e_mx < 2 * 2.0 ** -4
+
+
+def test_mx_and_fp32_scale_gemms_agree_when_every_scale_is_one():
+    """With every MX exponent byte 127 (scale 1) and every FP32 scale 1 the two
+    oracle GEMMs compute the same plain product of the codes: a cross-check of
+    the two independently written reductions and of their operand layouts."""
+    rng = np.random.default_rng(35)
+    M, K = 24, 384
+    x = _rand_codes(rng, (M, K))
+    w = _rand_codes(rng, (256, K))
+    ex = np.full((K // 128, M, 4), 127, dtype=np.uint8)
+    ew = np.full((K // 128, 256, 4), 127, dtype=np.uint8)
+    mx_val, mx_abs = oracle.mx_gemm(x, ex, w, ew)
+    sx = np.ones((K // 128, M), dtype=np.float32)
+    sw = np.ones((2, K // 128), dtype=np.float32)
+    bs_val, bs_abs = oracle.gemm_fprop(x, sx, w, sw)
+    assert np.allclose(mx_val, bs_val, rtol=0, atol=1e-12 * np.max(bs_abs))
+    assert np.allclose(mx_abs, bs_abs, rtol=1e-15, atol=0)
