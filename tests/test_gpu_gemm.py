@@ -151,13 +151,14 @@ def test_empty_reduction_writes_zeros(fb):
 
 def test_config_qkv_1p7b_fprop_from_real_distribution(fb):
     """Qwen3-1.7B QKV Fprop (M=8192, K=2048, N=4096): activations with outlier
-    channels quantized by the oracle, sampled 128x128 output tiles."""
+    channels quantized by the oracle, 64 seeded random 128x128 output tiles
+    plus the four corner tiles."""
     lin = synth.qkv_1p7b()
     xq, sx = oracle.quantize_rowwise(host_input(lin.x))
     wq, _, sw = oracle.quantize_weight_block(host_input(lin.w))
     y = _fprop(fb, xq, sx, wq, sw)
     rng = np.random.default_rng(23)
-    worst = check_gemm_tiles(y, oracle.gemm_fprop, (xq, sx, wq, sw), sample_tiles(rng, 8192, 4096, 12),
+    worst = check_gemm_tiles(y, oracle.gemm_fprop, (xq, sx, wq, sw), sample_tiles(rng, 8192, 4096, 64),
                              what="qkv fprop")
     assert worst <= 1.0
 
