@@ -281,6 +281,78 @@ def gemm_wgrad(dyqT, sdyT, xqT, sxT, rows=None, cols=None):
 
 
 # --------------------------------------------------------------------------
+# The same GEMMs with a float64 matmul as the chunk-sum step
+# --------------------------------------------------------------------------
+#
+# gemm_*_mm evaluate the definition above for the requested rows and columns
+# with one library step: the 128-term chunk sums P_c come from a float64
+# matmul of the decoded codes.  Every product of two E4M3 values and every
+# partial sum of one chunk is exact in binary64 (products carry at most 8
+# significant bits and span at most 2^36, so 128 of them need at most 51
+# bits), so P_c does not depend on the order the library adds in.  The scale
+# product (double(sA) * double(sB)), its product with P_c and the sum over
+# chunks in chunk order are the same binary64 operations, in the same order,
+# as the C routines perform, so the results are bit-identical to gemm_fprop /
+# gemm_dgrad / gemm_wgrad (tests/test_oracle_gemm.py checks that) at a
+# fraction of the cost on long reductions; the large-shape parity tests use
+# them.
+
+def _chunked_product(a, sa, b, sb):
+    """a [R, Kr] and b [C, Kr] codes (reduction contiguous), sa [Kr/128, R]
+    and sb [Kr/128, C] per-chunk scales (float32).  Returns (value, abs_sum),
+    each [R, C] float64: sum_c sa[c] sb[c] P_c and sum_c sa[c] sb[c] |.|_c."""
+    table = e4m3_table()
+    R, Kr = a.shape
+    C = b.shape[0]
+    KC = Kr // 128
+    av = table[a].reshape(R, KC, 128).transpose(1, 0, 2)
+    bv = table[b].reshape(C, KC, 128).transpose(1, 2, 0)
+    p = np.matmul(av, bv)                       # [KC, R, C], exact chunk sums
+    pa = np.matmul(np.abs(av), np.abs(bv))
+    sa64 = np.asarray(sa, dtype=np.float32).astype(np.float64)
+    sb64 = np.asarray(sb, dtype=np.float32).astype(np.float64)
+    val = np.zeros((R, C), dtype=np.float64)
+    absd = np.zeros((R, C), dtype=np.float64)
+    for c in range(KC):
+        scale = sa64[c][:, None] * sb64[c][None, :]
+        val += scale * p[c]
+        absd += scale * pa[c]
+    return val, absd
+
+
+def gemm_fprop_mm(xq, sx, wq, sw, rows=None, cols=None):
+    """gemm_fprop (same arguments and result) with a float64 matmul step."""
+    M, K = xq.shape
+    N = wq.shape[0]
+    rows = np.arange(M) if rows is None else np.asarray(rows)
+    cols = np.arange(N) if cols is None else np.asarray(cols)
+    sb = np.asarray(sw, dtype=np.float32)[cols // 128, :].T     # [K/128, len(cols)]
+    return _chunked_product(np.asarray(xq)[rows], np.asarray(sx)[:, rows], np.asarray(wq)[cols], sb)
+
+
+def gemm_dgrad_mm(dyq, sdy, wq, sw, rows=None, cols=None):
+    """gemm_dgrad (same arguments: wq in its natural [N, K] layout) with a
+    float64 matmul step."""
+    M, N = dyq.shape
+    K = wq.shape[1]
+    rows = np.arange(M) if rows is None else np.asarray(rows)
+    cols = np.arange(K) if cols is None else np.asarray(cols)
+    b = np.ascontiguousarray(np.asarray(wq)[:, cols].T)          # [len(cols), N]
+    sb = np.asarray(sw, dtype=np.float32)[:, cols // 128]        # [N/128, len(cols)]
+    return _chunked_product(np.asarray(dyq)[rows], np.asarray(sdy)[:, rows], b, sb)
+
+
+def gemm_wgrad_mm(dyqT, sdyT, xqT, sxT, rows=None, cols=None):
+    """gemm_wgrad (same arguments and result) with a float64 matmul step."""
+    N, M = dyqT.shape
+    K = xqT.shape[0]
+    rows = np.arange(N) if rows is None else np.asarray(rows)
+    cols = np.arange(K) if cols is None else np.asarray(cols)
+    return _chunked_product(np.asarray(dyqT)[rows], np.asarray(sdyT)[:, rows], np.asarray(xqT)[cols],
+                            np.asarray(sxT)[:, cols])
+
+
+# --------------------------------------------------------------------------
 # MX variant (power-of-two scales per 1x32 block)
 # --------------------------------------------------------------------------
 

@@ -272,3 +272,53 @@ def test_f32_tolerance_accepts_rounding_and_rejects_one_extra_ulp_of_s():
     summed = (base.astype(np.float64) + exact).astype(np.float32)
     ok, _, _ = oracle.gemm_check_f32(summed, exact, absd, base=base)
     assert ok
+
+
+# ---------------------------------------------------------------------------
+# The matmul-step forms (gemm_*_mm) against the literal C loops
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (256, 384, 640), (384, 256, 1024)])
+def test_matmul_step_forms_are_bit_identical_to_the_loops(M, N, K):
+    """Same definition, same binary64 operations outside the exact chunk
+    sums: values and |.|-sums must agree bit for bit on random codes of every
+    magnitude (subnormals and signed zeros included) and random scales, on
+    ragged row/column selections."""
+    rng = np.random.default_rng(M + 3 * N + 7 * K)
+    rows = np.sort(rng.choice(M, size=min(M, 96), replace=False))
+    cols = np.sort(rng.choice(N, size=min(N, 80), replace=False))
+    # Fprop: xq [M, K], wq [N, K]
+    xq, wq = _rand_codes(rng, (M, K)), _rand_codes(rng, (N, K))
+    sx, sw = _rand_scales(rng, (K // 128, M)), _rand_scales(rng, (N // 128, K // 128))
+    for got, want in zip(oracle.gemm_fprop_mm(xq, sx, wq, sw, rows, cols),
+                         oracle.gemm_fprop(xq, sx, wq, sw, rows, cols)):
+        assert np.array_equal(got.view(np.uint64), want.view(np.uint64))
+    # Dgrad: dyq [M, N] reduced over N, wq2 [N, K] natural layout
+    dyq, wq2 = _rand_codes(rng, (M, N)), _rand_codes(rng, (N, K))
+    sdy, sw2 = _rand_scales(rng, (N // 128, M)), _rand_scales(rng, (N // 128, K // 128))
+    kcols = np.sort(rng.choice(K, size=min(K, 72), replace=False))
+    for got, want in zip(oracle.gemm_dgrad_mm(dyq, sdy, wq2, sw2, rows, kcols),
+                         oracle.gemm_dgrad(dyq, sdy, wq2, sw2, rows, kcols)):
+        assert np.array_equal(got.view(np.uint64), want.view(np.uint64))
+    # Wgrad: dyqT [N, M], xqT [K, M] reduced over M
+    dyqT, xqT = _rand_codes(rng, (N, M)), _rand_codes(rng, (K, M))
+    sdyT, sxT = _rand_scales(rng, (M // 128, N)), _rand_scales(rng, (M // 128, K))
+    nrows = np.sort(rng.choice(N, size=min(N, 64), replace=False))
+    for got, want in zip(oracle.gemm_wgrad_mm(dyqT, sdyT, xqT, sxT, nrows, kcols),
+                         oracle.gemm_wgrad(dyqT, sdyT, xqT, sxT, nrows, kcols)):
+        assert np.array_equal(got.view(np.uint64), want.view(np.uint64))
+
+
+def test_matmul_step_form_on_a_long_reduction():
+    """A 4096-deep Wgrad reduction (32 chunks) with codes at the extremes of
+    the E4M3 range, where a chunk sum needs the most bits."""
+    rng = np.random.default_rng(77)
+    N, K, M = 128, 128, 4096
+    ext = np.array([0x01, 0x02, 0x7E, 0x7D, 0x81, 0xFE], dtype=np.uint8)
+    dyqT = rng.choice(ext, size=(N, M)).astype(np.uint8)
+    xqT = rng.choice(ext, size=(K, M)).astype(np.uint8)
+    sdyT, sxT = _rand_scales(rng, (M // 128, N)), _rand_scales(rng, (M // 128, K))
+    rows, cols = np.arange(0, N, 5), np.arange(0, K, 3)
+    for got, want in zip(oracle.gemm_wgrad_mm(dyqT, sdyT, xqT, sxT, rows, cols),
+                         oracle.gemm_wgrad(dyqT, sdyT, xqT, sxT, rows, cols)):
+        assert np.array_equal(got.view(np.uint64), want.view(np.uint64))
