@@ -52,8 +52,12 @@ sys.path.insert(0, ROOT)
 
 METRIC = "FP8 block-scaled GEMM TFLOP/s (incl. quantize) and % of B300 FP8 peak"
 UNIT = "TFLOP/s"
-TOKENS = {"layer_3p8b": 32768, "qkv_1p7b": 8192, "tiny": 256}
+TOKENS = {"layer_3p8b": 32768, "swiglu": 16384, "up_bwd": 16384, "qkv_1p7b": 8192, "tiny": 256}
+# the GEMMs each linear of a workload runs in one step
+WORKLOAD_GEMMS = {"layer_3p8b": ("fprop", "dgrad", "wgrad"), "swiglu": ("fprop",), "up_bwd": ("dgrad", "wgrad"),
+                  "qkv_1p7b": ("fprop",), "tiny": ("fprop",)}
 FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 / 2.25 PFLOP/s)
+NOMINAL_FP8_TFLOPS = 4500.0
 VARIANTS = {
     "fp32-scale": "FP32 scale amax/448 per 1x128 tile (X, dY) and 128x128 block (W); per-128-chunk promotion",
     "mx": ("MX variant: power-of-two (E8M0) scale per 1x32 block along each GEMM's reduction dim, "
@@ -87,6 +91,10 @@ def workload_shapes(name, tokens=None):
     M = tokens or TOKENS[name]
     if name == "layer_3p8b":
         return [(n, M, K, N) for n, K, N in synth.LAYER_3P8B]
+    if name == "swiglu":
+        return [("gate_up", M, 2048, 12288), ("down", M, 6144, 2048)]
+    if name == "up_bwd":
+        return [("up", M, 2048, 6144)]
     if name == "qkv_1p7b":
         return [("qkv", M, 2048, 4096)]
     return [("tiny", M, 512, 384)]
@@ -97,30 +105,38 @@ def workload_config(name, tokens=None):
     desc = {
         "layer_3p8b": "3.8B-shaped layer: QKV 3072->4608, O 3072->3072, gate+up 3072->16384, down 8192->3072; "
                       "Fprop+Dgrad+Wgrad each with all quantizers",
-        "qkv_1p7b": "Qwen3-1.7B QKV layer 2048->4096; Fprop+Dgrad+Wgrad with all quantizers",
-        "tiny": "tiny 512 -> 384 layer; Fprop+Dgrad+Wgrad with all quantizers",
+        "swiglu": "SwiGLU MLP forward: gate+up 2048->12288 Fprop, SwiGLU fused into the down projection's "
+                  "row+column quantizer, down 6144->2048 Fprop; weight and input quantizers included",
+        "up_bwd": "backward of the 2048->6144 up-projection: row+column pass over dY, column-wise pass over X, "
+                  "Dgrad (reduce 6144) and Wgrad (reduce over the tokens); the weight codes come from the "
+                  "forward pass and are not re-quantized in the step",
+        "qkv_1p7b": "Qwen3-1.7B QKV Fprop 2048->4096: weight-block and row-wise quantizers, Fprop",
+        "tiny": "tiny Fprop: FP32 A 256x512, B 512x384 (W = B^T): weight-block and row-wise quantizers, Fprop",
     }[name]
-    return {"workload": name, "description": desc, "tokens": shapes[0][1],
+    return {"workload": name, "description": desc, "tokens": shapes[0][1], "gemms": list(WORKLOAD_GEMMS[name]),
             "linears": {n: {"M": M, "K": K, "N": N} for n, M, K, N in shapes}}
 
 
-def step_flops(shapes):
-    return sum(3 * 2 * M * N * K for _, M, K, N in shapes)
+def step_flops(shapes, gemms=("fprop", "dgrad", "wgrad")):
+    return sum(len(gemms) * 2 * M * N * K for _, M, K, N in shapes)
 
 
 def make_inputs(name, device, tokens=None):
-    """BF16 X, W, dY per linear, generated on `device`."""
+    """Input tensors per linear (X, W, dY as the workload needs), generated on `device`."""
     from fp8_precision_pretraining_amax_b300 import synth
     M = tokens or TOKENS[name]
     if name == "layer_3p8b":
         return synth.layer_3p8b(device, M=M)
+    if name == "swiglu":
+        return list(synth.swiglu(device, M=M))
+    if name == "up_bwd":
+        return [synth.up_bwd(device, M=M)]
     if name == "qkv_1p7b":
-        lin = synth.qkv_1p7b(device, M=M)
-        lin.dy = synth.grads(lin.M, lin.N, synth.generator(11, device), device)
-        return [lin]
-    gen = synth.generator(0, device)
-    return [synth.Linear("tiny", M, 512, 384, x=synth.activations(M, 512, gen, device),
-                         w=synth.weight(384, 512, gen, device), dy=synth.grads(M, 384, gen, device))]
+        return [synth.qkv_1p7b(device, M=M)]
+    lin = synth.tiny(device)
+    gen = synth.generator(10, device)
+    lin.dy = synth.grads(lin.M, lin.N, gen, device)   # used by the layer step of the MX variant / CPU sample
+    return [lin]
 
 
 # ---------------------------------------------------------------------------
@@ -226,18 +242,39 @@ def gemm_traffic_record(variant="fp32-scale"):
 # our arm
 # ---------------------------------------------------------------------------
 
+def rowcol_bytes(R, C):
+    """Row+column pass over BF16 [R, C]: one read, two code layouts, two scale sets."""
+    return 2 * R * C + 2 * R * C + 4 * R * (C // 128) + 4 * (R // 128) * C
+
+
+def rowwise_bytes(R, C, in_bytes=2):
+    return in_bytes * R * C + R * C + 4 * R * (C // 128)
+
+
+def colwise_bytes(R, C, in_bytes=2):
+    return in_bytes * R * C + R * C + 4 * (R // 128) * C
+
+
+def weight_bytes(N, K, transposed=True, in_bytes=2):
+    return in_bytes * N * K + (2 if transposed else 1) * N * K + 4 * (N // 128) * (K // 128)
+
+
+def swiglu_bytes(M, F):
+    """SwiGLU-fused quantizer: reads g and u (BF16), writes H's row-wise and
+    column-wise codes and scales."""
+    return 4 * M * F + 2 * M * F + 4 * M * (F // 128) + 4 * (M // 128) * F
+
+
 def step_launches(fp8bq, L, lin):
     """(kind, algorithmic work, call) for one linear's 6 launches, in step order.
     Work: FLOPs for GEMMs, bytes read + written for quantizers (BF16 in, one
     code byte per layout, one FP32 scale per 128 elements and layout)."""
     M, K, N = L.M, L.K, L.N
-    rowcol = lambda R, C: 2 * R * C + 2 * R * C + 4 * R * (C // 128) + 4 * (R // 128) * C
     return [
-        ("quant_weight", 2 * N * K + 2 * N * K + 4 * (N // 128) * (K // 128),
-         lambda: fp8bq.fp8bq_quantize_weight_block(lin.w, L.wq, L.wqT, L.sw)),
-        ("quant_rowcol", rowcol(M, K), lambda: fp8bq.fp8bq_quantize_rowcol(lin.x, L.xq, L.sx, L.xqT, L.sxT)),
+        ("quant_weight", weight_bytes(N, K), lambda: fp8bq.fp8bq_quantize_weight_block(lin.w, L.wq, L.wqT, L.sw)),
+        ("quant_rowcol", rowcol_bytes(M, K), lambda: fp8bq.fp8bq_quantize_rowcol(lin.x, L.xq, L.sx, L.xqT, L.sxT)),
         ("gemm_fprop", 2 * M * N * K, lambda: fp8bq.fp8bq_gemm_fprop(L.xq, L.sx, L.wq, L.sw, L.y)),
-        ("quant_rowcol", rowcol(M, N),
+        ("quant_rowcol", rowcol_bytes(M, N),
          lambda: fp8bq.fp8bq_quantize_rowcol(lin.dy, L.dyq, L.sdy, L.dyqT, L.sdyT)),
         ("gemm_dgrad", 2 * M * N * K, lambda: fp8bq.fp8bq_gemm_dgrad(L.dyq, L.sdy, L.wqT, L.sw, L.dx)),
         ("gemm_wgrad", 2 * M * N * K, lambda: fp8bq.fp8bq_gemm_wgrad(L.dyqT, L.sdyT, L.xqT, L.sxT, L.dw)),
@@ -260,26 +297,112 @@ def step_launches_mx(fp8bq, L, lin):
     ]
 
 
+class Unit:
+    """One part of the step: its launches, the input tensors a user would
+    bring from the host and the outputs a user would take back (the
+    end-to-end leg moves exactly these)."""
+
+    def __init__(self, name, launches, inputs, outputs, setup=()):
+        self.name, self.launches, self.inputs, self.outputs = name, launches, list(inputs), list(outputs)
+        self.setup = list(setup)   # calls made once before the first step (not timed)
+
+
+def data_parallel_wgrad(fp8bq, L, launches, dist):
+    """N > 1: the rank's Wgrad in FP32 (fp8bq_gemm_wgrad_f32) and one NCCL
+    all-reduce of it, in place of the BF16 Wgrad.  Returns the FP32 dW."""
+    import torch
+    dw32 = torch.empty((L.N, L.K), dtype=torch.float32, device=L.dw.device)
+    i = [k for k, _, _ in launches].index("gemm_wgrad")
+    launches[i] = ("gemm_wgrad", launches[i][1],
+                   lambda: fp8bq.fp8bq_gemm_wgrad_f32(L.dyqT, L.sdyT, L.xqT, L.sxT, dw32))
+    launches.insert(i + 1, ("comm_allreduce_dw", 4 * L.N * L.K,
+                            lambda: dist.all_reduce(dw32, op=dist.ReduceOp.SUM)))
+    return dw32
+
+
+def build_units(fp8bq, name, lins, dev, world, variant="fp32-scale"):
+    """The step of workload `name` as a list of Units."""
+    import torch
+    import torch.distributed as dist
+    from fp8_precision_pretraining_amax_b300.linear import LinearFP8, LinearMX, SwiGLUMLPFP8
+    mx = variant == "mx"
+    if mx and name != "layer_3p8b":
+        raise SystemExit("the MX variant is benchmarked on the layer_3p8b workload only")
+    units = []
+    if name == "layer_3p8b":
+        for lin in lins:
+            L = (LinearMX if mx else LinearFP8)(lin.M, lin.K, lin.N, device=dev)
+            launches = (step_launches_mx if mx else step_launches)(fp8bq, L, lin)
+            dw = L.dw
+            if world > 1 and mx:  # the MX variant has no FP32 Wgrad: its BF16 dW is summed
+                launches.append(("comm_allreduce_dw", 2 * L.N * L.K,
+                                 lambda L=L: dist.all_reduce(L.dw, op=dist.ReduceOp.SUM)))
+            elif world > 1:
+                dw = data_parallel_wgrad(fp8bq, L, launches, dist)
+            units.append(Unit(lin.name, launches, (lin.x, lin.w, lin.dy), (L.y, L.dx, dw)))
+    elif name == "swiglu":
+        gu_lin, down_lin = lins
+        M, D, F = gu_lin.M, gu_lin.K, down_lin.K
+        mlp = SwiGLUMLPFP8(M, D, F, device=dev)
+        g = mlp.gate_up
+        launches = [
+            ("quant_weight", weight_bytes(2 * F, D, transposed=False),
+             lambda: fp8bq.fp8bq_quantize_weight_block(gu_lin.w, g.wq, None, g.sw)),
+            ("quant_rowwise", rowwise_bytes(M, D), lambda: fp8bq.fp8bq_quantize_rowwise(gu_lin.x, g.xq, g.sx)),
+            ("gemm_fprop", 2 * M * 2 * F * D, lambda: fp8bq.fp8bq_gemm_fprop(g.xq, g.sx, g.wq, g.sw, g.y)),
+            ("quant_swiglu", swiglu_bytes(M, F),
+             lambda: fp8bq.fp8bq_swiglu_quantize(g.y, None, mlp.hq, mlp.sh, mlp.hqT, mlp.shT)),
+            ("quant_weight", weight_bytes(D, F, transposed=False),
+             lambda: fp8bq.fp8bq_quantize_weight_block(down_lin.w, mlp.wdq, None, mlp.swd)),
+            ("gemm_fprop", 2 * M * D * F, lambda: fp8bq.fp8bq_gemm_fprop(mlp.hq, mlp.sh, mlp.wdq, mlp.swd, mlp.out)),
+        ]
+        units.append(Unit("mlp", launches, (gu_lin.x, gu_lin.w, down_lin.w), (mlp.out,)))
+    elif name == "up_bwd":
+        lin = lins[0]
+        M, K, N = lin.M, lin.K, lin.N
+        L = LinearFP8(M, K, N, device=dev)
+        launches = [
+            ("quant_colwise", colwise_bytes(M, K), lambda: fp8bq.fp8bq_quantize_colwise(lin.x, L.xqT, L.sxT)),
+            ("quant_rowcol", rowcol_bytes(M, N),
+             lambda: fp8bq.fp8bq_quantize_rowcol(lin.dy, L.dyq, L.sdy, L.dyqT, L.sdyT)),
+            ("gemm_dgrad", 2 * M * N * K, lambda: fp8bq.fp8bq_gemm_dgrad(L.dyq, L.sdy, L.wqT, L.sw, L.dx)),
+            ("gemm_wgrad", 2 * M * N * K, lambda: fp8bq.fp8bq_gemm_wgrad(L.dyqT, L.sdyT, L.xqT, L.sxT, L.dw)),
+        ]
+        dw = data_parallel_wgrad(fp8bq, L, launches, dist) if world > 1 else L.dw
+        # the weight's codes (and transposed codes) come from the forward pass
+        setup = [lambda: fp8bq.fp8bq_quantize_weight_block(lin.w, L.wq, L.wqT, L.sw)]
+        units.append(Unit(lin.name, launches, (lin.x, lin.dy), (L.dx, dw), setup=setup))
+    else:  # Fprop only: qkv_1p7b, tiny
+        lin = lins[0]
+        M, K, N = lin.M, lin.K, lin.N
+        L = LinearFP8(M, K, N, device=dev)
+        eb = lin.x.element_size()
+        launches = [
+            ("quant_weight", weight_bytes(N, K, transposed=False, in_bytes=eb),
+             lambda: fp8bq.fp8bq_quantize_weight_block(lin.w, L.wq, None, L.sw)),
+            ("quant_rowwise", rowwise_bytes(M, K, in_bytes=eb), lambda: fp8bq.fp8bq_quantize_rowwise(lin.x, L.xq, L.sx)),
+            ("gemm_fprop", 2 * M * N * K, lambda: fp8bq.fp8bq_gemm_fprop(L.xq, L.sx, L.wq, L.sw, L.y)),
+        ]
+        units.append(Unit(lin.name, launches, (lin.x, lin.w), (L.y,)))
+    return units
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     from fp8_precision_pretraining_amax_b300 import fp8bq
-    from fp8_precision_pretraining_amax_b300.linear import LinearFP8, LinearMX
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     shapes = workload_shapes(args.workload, args.tokens)
     lins = make_inputs(args.workload, dev, args.tokens)
     mx = args.variant == "mx"
-    layers = [(LinearMX if mx else LinearFP8)(l.M, l.K, l.N, device=dev) for l in lins]
-    plan = [(step_launches_mx if mx else step_launches)(fp8bq, L, lin) for L, lin in zip(layers, lins)]
-    if world > 1:
-        # data parallel: each rank's batch gives a partial dW; the ranks sum
-        # them (NCCL all-reduce of the BF16 dW of every linear, each step)
-        for L, launches in zip(layers, plan):
-            launches.append(("comm_allreduce_dw", 2 * L.N * L.K,
-                             lambda L=L: torch.distributed.all_reduce(L.dw, op=torch.distributed.ReduceOp.SUM)))
+    units = build_units(fp8bq, args.workload, lins, dev, world, args.variant)
+    for u in units:
+        for fn in u.setup:
+            fn()
+    plan = [u.launches for u in units]
     torch.cuda.synchronize()
-    flops = step_flops(shapes)
+    flops = step_flops(shapes, WORKLOAD_GEMMS[args.workload])
     launches_per_step = sum(1 for p in plan for kind, _, _ in p if not kind.startswith("comm"))
 
     def barrier():
@@ -339,13 +462,13 @@ def run_ours(args, rank, world, local_rank):
     ms_per_step = dev_ms / args.steps
     value = flops * world * args.steps / (dev_ms * 1e-3) / 1e12
 
-    e2e = None if args.no_e2e else run_e2e(args, lins, layers, dev, flops, world, barrier)
+    e2e = None if args.no_e2e else run_e2e(args, units, dev, flops, world, barrier)
 
     if rank != 0:
         return None
     pk = peaks()
-    fp8_sus = pk["bf16_sustained"] * FP8_OVER_BF16
     fp8_burst = pk["bf16_burst"] * FP8_OVER_BF16
+    fp8_sus = pk["bf16_sustained"] * FP8_OVER_BF16
     gk = [v for k, v in per_kind.items() if k.startswith("gemm")]
     qk = [v for k, v in per_kind.items() if k.startswith("quant")]
     g_ms, g_fl, g_n = sum(v["ms"] for v in gk), sum(v["work"] for v in gk), sum(v["launches"] for v in gk)
@@ -360,18 +483,24 @@ def run_ours(args, rank, world, local_rank):
         b = {"launches_per_step": v["launches"] // args.steps, "ms_per_step": v["ms"] / args.steps}
         if k.startswith("gemm"):
             b["tflops"] = v["work"] / (v["ms"] * 1e-3) / 1e12
-        else:
+            b["frac_of_fp8_peak"] = b["tflops"] / fp8_burst
+        elif k.startswith("quant"):
             b["gbs"] = v["work"] / (v["ms"] * 1e-3) / 1e9
             b["frac_of_hbm"] = b["gbs"] / pk["hbm_gbs"]
         breakdown[k] = b
     breakdown["gemm_only_tflops"] = achieved
-    breakdown["quantizers"] = {"gbs": q_by / (q_ms * 1e-3) / 1e9,
-                               "frac_of_hbm": q_by / (q_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
-                               "ms_per_step": q_ms / args.steps}
+    if qk:
+        breakdown["quantizers"] = {"gbs": q_by / (q_ms * 1e-3) / 1e9,
+                                   "frac_of_hbm": q_by / (q_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                                   "ms_per_step": q_ms / args.steps}
     cfg = workload_config(args.workload, args.tokens)
     cfg["variant"] = VARIANTS[args.variant]
-    cfg["parallelism"] = (f"data parallel x{world}: own batch per rank, dW all-reduced each step"
-                          if world > 1 else "single GPU")
+    if world > 1:
+        cfg["parallelism"] = (f"data parallel x{world}: own batch per rank"
+                              + (", FP32 dW all-reduced each step" if "wgrad" in WORKLOAD_GEMMS[args.workload]
+                                 else " (replicas: no exchange on this path)"))
+    else:
+        cfg["parallelism"] = "single GPU"
     cfg["l2"] = "inputs larger than L2 (no flush)" if args.workload != "tiny" else "inputs fit in L2"
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -380,14 +509,17 @@ def run_ours(args, rank, world, local_rank):
         "dtype": ("e4m3 (e8m0 block scales) x e4m3 -> f32 accumulate -> bf16" if mx
                   else "e4m3 x e4m3 -> f32 accumulate -> bf16"), "data": "synthetic",
         "config": cfg,
-        "pct_of_fp8_peak": 100.0 * value / fp8_sus,
+        "pct_of_fp8_peak": 100.0 * value / fp8_burst,
+        "pct_of_nominal_fp8_peak": 100.0 * value / NOMINAL_FP8_TFLOPS,
         "roofline": {"bound": "tensor",
                      "kernel": ("mx_gemm_kernel (Fprop/Dgrad/Wgrad)" if mx
                                 else "gemm_block_scaled_kernel (Fprop/Dgrad/Wgrad)"),
-                     "achieved": achieved, "peak": fp8_sus, "unit": "TFLOP/s", "frac": achieved / fp8_sus,
+                     "achieved": achieved, "peak": fp8_burst, "unit": "TFLOP/s", "frac": achieved / fp8_burst,
                      "traffic": traffic,
-                     "peak_note": (f"FP8 = 2 x {pk['source']} sustained cuBLAS bf16 ({pk['bf16_sustained']} "
-                                   f"TFLOP/s); the burst-based FP8 peak would be {fp8_burst:.0f}"),
+                     "peak_note": (f"FP8 = 2 x {pk['source']} burst cuBLAS bf16 ({pk['bf16_burst']} TFLOP/s; "
+                                   f"the timed region is well under a second at near-maximum SM clock); "
+                                   f"sustained-based {fp8_sus:.0f}, nominal dense FP8 {NOMINAL_FP8_TFLOPS:.0f}: "
+                                   f"frac {achieved / fp8_sus:.3f} and {achieved / NOMINAL_FP8_TFLOPS:.3f}"),
                      "launches_per_step": g_n // args.steps},
         "breakdown": breakdown,
         "gpu_launches": launches_per_step * args.steps,
@@ -395,30 +527,29 @@ def run_ours(args, rank, world, local_rank):
     }
     if e2e is not None:
         out["e2e"] = e2e
-    if not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(lins, variant=args.variant)
+    if not args.no_cpu_baseline and world == 1:
+        out["cpu_baseline"] = cpu_baseline(args.workload, lins, variant=args.variant)
     return out
 
 
-def run_e2e(args, lins, layers, dev, flops, world, barrier):
-    """Same step through the Python API from pinned host buffers and back."""
+def run_e2e(args, units, dev, flops, world, barrier):
+    """The same step from pinned host buffers and back: every step copies each
+    unit's inputs host -> device into the tensors its launches read and its
+    outputs device -> host."""
     import torch
     from fp8_precision_pretraining_amax_b300 import fp8bq
 
-    host_in = [(l.x.cpu().pin_memory(), l.w.cpu().pin_memory(), l.dy.cpu().pin_memory()) for l in lins]
-    host_out = [(torch.empty(L.y.shape, dtype=torch.bfloat16).pin_memory(),
-                 torch.empty(L.dx.shape, dtype=torch.bfloat16).pin_memory(),
-                 torch.empty(L.dw.shape, dtype=torch.bfloat16).pin_memory()) for L in layers]
-    dev_in = [(torch.empty_like(l.x), torch.empty_like(l.w), torch.empty_like(l.dy)) for l in lins]
-    h2d = sum(t.numel() * t.element_size() for trio in host_in for t in trio)
-    d2h = sum(t.numel() * t.element_size() for trio in host_out for t in trio)
+    host_in = [[t.cpu().pin_memory() for t in u.inputs] for u in units]
+    host_out = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in u.outputs] for u in units]
+    h2d = sum(t.numel() * t.element_size() for hs in host_in for t in hs)
+    d2h = sum(t.numel() * t.element_size() for hs in host_out for t in hs)
 
-    # Three streams: host->device copies of linear i+1 and device->host copies
-    # of linear i-1 run while linear i computes (PCIe is full duplex).  Events
-    # keep each buffer's reuse in order across linears and steps.
+    # Three streams: host->device copies of unit i+1 and device->host copies
+    # of unit i-1 run while unit i computes (PCIe is full duplex).  Events
+    # keep each buffer's reuse in order across units and steps.
     comp = torch.cuda.current_stream(dev)
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    n = len(layers)
+    n = len(units)
     ev_in = [torch.cuda.Event() for _ in range(n)]
     ev_comp = [torch.cuda.Event() for _ in range(n)]
     ev_out = [torch.cuda.Event() for _ in range(n)]
@@ -427,25 +558,21 @@ def run_e2e(args, lins, layers, dev, flops, world, barrier):
         ev_out[i].record(s_out)
 
     def e2e_step():
-        for i, ((hx, hw, hdy), (dx_, dw_, ddy), L, (oy, odx, odw)) in enumerate(
-                zip(host_in, dev_in, layers, host_out)):
+        for i, (u, hin, hout) in enumerate(zip(units, host_in, host_out)):
             with torch.cuda.stream(s_in):
                 s_in.wait_event(ev_comp[i])          # last step's compute has read these inputs
-                dx_.copy_(hx, non_blocking=True)
-                dw_.copy_(hw, non_blocking=True)
-                ddy.copy_(hdy, non_blocking=True)
+                for d, h in zip(u.inputs, hin):
+                    d.copy_(h, non_blocking=True)
                 ev_in[i].record(s_in)
             comp.wait_event(ev_in[i])
             comp.wait_event(ev_out[i])               # last step's outputs have left the device
-            L.step(dx_, dw_, ddy)
-            if world > 1:
-                torch.distributed.all_reduce(L.dw, op=torch.distributed.ReduceOp.SUM)
+            for _, _, fn in u.launches:
+                fn()
             ev_comp[i].record(comp)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_comp[i])
-                oy.copy_(L.y, non_blocking=True)
-                odx.copy_(L.dx, non_blocking=True)
-                odw.copy_(L.dw, non_blocking=True)
+                for h, d in zip(hout, u.outputs):
+                    h.copy_(d, non_blocking=True)
                 ev_out[i].record(s_out)
 
     for _ in range(2):
@@ -467,8 +594,9 @@ def run_e2e(args, lins, layers, dev, flops, world, barrier):
         dt = float(t.item())
     return {"value": flops * world * steps / dt / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": 1e3 * dt / steps,
-            "path": (f"pinned host -> device copies, {type(layers[0]).__name__}.step (C-ABI), device -> pinned "
-                     "host copies; copies of neighbouring linears overlap compute on separate streams")}
+            "path": ("pinned host -> device copies of each unit's inputs, the unit's C-ABI launches, device -> "
+                     "pinned host copies of its outputs; copies of neighbouring units overlap compute on "
+                     "separate streams")}
 
 
 # ---------------------------------------------------------------------------
@@ -476,34 +604,54 @@ def run_e2e(args, lins, layers, dev, flops, world, barrier):
 # ---------------------------------------------------------------------------
 
 def host_slices(lins, tile):
-    """The operand slices the oracle sample needs, copied to the host."""
+    """The operand slices the oracle sample needs, copied to the host (a
+    missing operand of the workload gives None)."""
     from fp8_precision_pretraining_amax_b300 import synth
+
+    def bits(t):
+        if t is None:
+            return None
+        return synth.bf16_bits(t) if t.dtype == synth.torch.bfloat16 else t.detach().cpu().contiguous().numpy()
     out = []
     for l in lins:
+        dy = getattr(l, "dy", None)
         out.append(((l.name, l.M, l.K, l.N), (
-            synth.bf16_bits(l.x[:tile]),                    # tile rows of X, all K
-            synth.bf16_bits(l.x[:, :128].contiguous()),     # 128 columns of X, all tokens
-            synth.bf16_bits(l.w[:128]),                     # one N block of W, all K
-            synth.bf16_bits(l.w[:, :128].contiguous()),     # one K block of W, all N
-            synth.bf16_bits(l.dy[:tile]),                   # tile rows of dY
-            synth.bf16_bits(l.dy[:, :128].contiguous()))))  # 128 columns of dY, all tokens
+            bits(l.x[:tile]),                                         # tile rows of X, all K
+            bits(l.x[:, :128].contiguous()),                          # 128 columns of X, all tokens
+            bits(l.w[:128]),                                          # one N block of W, all K
+            bits(l.w[:, :128].contiguous()),                          # one K block of W, all N
+            None if dy is None else bits(dy[:tile]),                  # tile rows of dY
+            None if dy is None else bits(dy[:, :128].contiguous())))) # 128 columns of dY, all tokens
     return out
 
 
-def oracle_sample(slices, tile, variant="fp32-scale"):
+def quantized_elements(workload, lin_name, M, K, N):
+    """Elements the step's quantizers process for one linear, one layout pass
+    each (the oracle quantizes every layout separately)."""
+    if workload == "layer_3p8b":
+        return 2 * M * K + 2 * M * N + N * K      # X rows+cols, dY rows+cols, W
+    if workload == "up_bwd":
+        return M * K + 2 * M * N                  # X cols, dY rows+cols
+    if workload == "swiglu" and lin_name == "down":
+        return 2 * M * K + N * K                  # H rows+cols, W
+    return M * K + N * K                          # X rows, W
+
+
+def oracle_sample(slices, tile, variant="fp32-scale", workload="layer_3p8b"):
     """Time the oracle on a bounded sample of one step and extrapolate.
 
     For each linear: quantize the operand slices that one tile x tile output
-    block of Fprop, Dgrad and Wgrad needs, then compute those three blocks.
+    block of each of the workload's GEMMs needs, then compute those blocks.
     Quantizer seconds per element and GEMM seconds per multiply-add are
     scaled to the full step's element and multiply-add counts."""
     import numpy as np
     import oracle
 
+    gemms = WORKLOAD_GEMMS[workload]
     q_time = g_time = 0.0
     q_elems = g_macs = full_q = full_macs = 0
-    for (_, M, K, N), (xr, xc, wr, wc, dyr, dyc) in slices:
-        full_macs += 3 * M * N * K
+    for (name, M, K, N), (xr, xc, wr, wc, dyr, dyc) in slices:
+        full_macs += len(gemms) * M * N * K
         idx = np.arange(tile)
         if variant == "mx":
             full_q += 2 * M * K + 2 * M * N + 2 * N * K  # every operand in both layouts
@@ -515,39 +663,57 @@ def oracle_sample(slices, tile, variant="fp32-scale"):
             dyqT = oracle.mx_quantize_colwise(dyc)
             xqT = oracle.mx_quantize_colwise(xc)
             q_time += time.perf_counter() - t
+            q_elems += xr.size + wr.size + dyr.size + wc.size + dyc.size + xc.size
             t = time.perf_counter()
             oracle.mx_gemm(*xq, *wq, rows=idx, cols=idx)
             oracle.mx_gemm(*dyq, *wqT, rows=idx, cols=idx)
             oracle.mx_gemm(*dyqT, *xqT, rows=idx, cols=idx)
             g_time += time.perf_counter() - t
-        else:
-            full_q += 2 * M * K + 2 * M * N + N * K  # row-wise X, dY; column-wise dY, X; weight
+            g_macs += tile * tile * (K + N + M)
+            continue
+        full_q += quantized_elements(workload, name, M, K, N)
+        if "fprop" in gemms:
             t = time.perf_counter()
             xq, sx = oracle.quantize_rowwise(xr)
             wq, _, sw = oracle.quantize_weight_block(wr)
+            q_time += time.perf_counter() - t
+            q_elems += xr.size + wr.size
+            t = time.perf_counter()
+            oracle.gemm_fprop(xq, sx, wq, sw, rows=idx, cols=idx)
+            g_time += time.perf_counter() - t
+            g_macs += tile * tile * K
+        if "dgrad" in gemms:
+            t = time.perf_counter()
             dyq, sdy = oracle.quantize_rowwise(dyr)
             wq2, _, sw2 = oracle.quantize_weight_block(wc)
+            q_time += time.perf_counter() - t
+            q_elems += dyr.size + wc.size
+            t = time.perf_counter()
+            oracle.gemm_dgrad(dyq, sdy, wq2, sw2, rows=idx, cols=idx)
+            g_time += time.perf_counter() - t
+            g_macs += tile * tile * N
+        if "wgrad" in gemms:
+            t = time.perf_counter()
             dyqT, sdyT = oracle.quantize_colwise(dyc)
             xqT, sxT = oracle.quantize_colwise(xc)
             q_time += time.perf_counter() - t
+            q_elems += dyc.size + xc.size
             t = time.perf_counter()
-            oracle.gemm_fprop(xq, sx, wq, sw, rows=idx, cols=idx)
-            oracle.gemm_dgrad(dyq, sdy, wq2, sw2, rows=idx, cols=idx)
             oracle.gemm_wgrad(dyqT, sdyT, xqT, sxT, rows=idx, cols=idx)
             g_time += time.perf_counter() - t
-        q_elems += xr.size + wr.size + dyr.size + wc.size + dyc.size + xc.size
-        g_macs += tile * tile * (K + N + M)
+            g_macs += tile * tile * M
     est = full_q * (q_time / q_elems) + full_macs * (g_time / g_macs)
     return {"tflops": 2 * full_macs / est / 1e12, "sample_seconds": q_time + g_time, "step_seconds": est}
 
 
-def cpu_baseline(lins, tile=64, variant="fp32-scale"):
+def cpu_baseline(workload, lins, tile=64, variant="fp32-scale"):
     import oracle
-    r = oracle_sample(host_slices(lins, tile), tile, variant)
+    r = oracle_sample(host_slices(lins, tile), tile, variant, workload)
+    gem = "/".join(g.capitalize() for g in WORKLOAD_GEMMS[workload])
     return {"value": r["tflops"], "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": (f"per linear one {tile}x{tile} output block of Fprop, Dgrad and Wgrad plus the "
-                       f"quantization of the operand slices it needs ({r['sample_seconds']:.1f} s of CPU "
-                       f"work), extrapolated to the full step ({r['step_seconds']:.0f} s)")}
+            "sample": (f"per linear one {tile}x{tile} output block of {gem} plus the quantization of the "
+                       f"operand slices it needs ({r['sample_seconds']:.1f} s of CPU work), extrapolated to the "
+                       f"full step ({r['step_seconds']:.0f} s)")}
 
 
 def run_reference(args):
@@ -559,14 +725,16 @@ def run_reference(args):
     lins = make_inputs(args.workload, device, args.tokens)
     sl = host_slices(lins, tile)
     del lins
-    vals = [oracle_sample(sl, tile, args.variant) for _ in range(args.warmup + args.steps)][args.warmup:]
+    vals = [oracle_sample(sl, tile, args.variant, args.workload) for _ in range(args.warmup + args.steps)]
+    vals = vals[args.warmup:]
     value = statistics.median(v["tflops"] for v in vals)
     est = statistics.median(v["step_seconds"] for v in vals)
     cfg = workload_config(args.workload, args.tokens)
     cfg["variant"] = VARIANTS[args.variant]
     cfg["parallelism"] = "host cores (oracle)"
-    sample = (f"each step: per linear one {tile}x{tile} output block of Fprop, Dgrad and Wgrad plus the "
-              f"quantization of the operand slices it needs; time extrapolated to the full step")
+    gem = "/".join(g.capitalize() for g in WORKLOAD_GEMMS[args.workload])
+    sample = (f"each step: per linear one {tile}x{tile} output block of {gem} plus the quantization of the "
+              f"operand slices it needs; time extrapolated to the full step")
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": est * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None,

@@ -69,3 +69,51 @@ def test_reference_arm_prints_one_json_line(variant):
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["config"]["workload"] == "tiny" and d["config"]["variant"] == bench.VARIANTS[variant]
+
+
+class _Lin:
+    def __init__(self, name, M, K, N, x=True, dy=True):
+        import torch
+        self.name, self.M, self.K, self.N = name, M, K, N
+        self.x = torch.zeros((M, K), dtype=torch.bfloat16)
+        self.w = torch.zeros((N, K), dtype=torch.bfloat16)
+        self.dy = torch.zeros((M, N), dtype=torch.bfloat16) if dy else None
+
+
+@pytest.mark.parametrize("workload", ["layer_3p8b", "swiglu", "up_bwd", "qkv_1p7b", "tiny"])
+def test_every_workload_plan_does_its_gemms_once(workload):
+    """Each workload's step runs exactly the GEMMs its configuration names
+    (2 M N K each), and the end-to-end leg moves the inputs and outputs of
+    every unit.  Plans are built on CPU tensors; no launch is made."""
+    from fp8_precision_pretraining_amax_b300 import fp8bq
+    shapes = bench.workload_shapes(workload, tokens=256)
+    lins = [_Lin(n, M, K, N) for n, M, K, N in shapes]
+    units = bench.build_units(fp8bq, workload, lins, "cpu", 1)
+    kinds = [k for u in units for k, _, _ in u.launches]
+    gemm_flops = sum(w for u in units for k, w, _ in u.launches if k.startswith("gemm"))
+    assert gemm_flops == bench.step_flops(shapes, bench.WORKLOAD_GEMMS[workload])
+    want = {"layer_3p8b": 12, "swiglu": 2, "up_bwd": 2, "qkv_1p7b": 1, "tiny": 1}[workload]
+    assert sum(k.startswith("gemm") for k in kinds) == want
+    assert not any(k.startswith("comm") for k in kinds)
+    assert all(u.inputs and u.outputs for u in units)
+    if workload == "swiglu":
+        assert kinds == ["quant_weight", "quant_rowwise", "gemm_fprop", "quant_swiglu", "quant_weight", "gemm_fprop"]
+    if workload == "up_bwd":
+        assert kinds == ["quant_colwise", "quant_rowcol", "gemm_dgrad", "gemm_wgrad"]
+        assert len(units[0].setup) == 1    # the weight codes come from the forward pass, outside the step
+
+
+def test_data_parallel_plan_all_reduces_the_fp32_wgrad():
+    """N > 1: every Wgrad is computed in FP32 and all-reduced right after
+    (the same arithmetic as dp.LinearFP8DP); the GEMM count is unchanged."""
+    import torch
+    from fp8_precision_pretraining_amax_b300 import fp8bq
+    shapes = bench.workload_shapes("layer_3p8b", tokens=256)
+    lins = [_Lin(n, M, K, N) for n, M, K, N in shapes]
+    units = bench.build_units(fp8bq, "layer_3p8b", lins, "cpu", 2)
+    for u in units:
+        kinds = [k for k, _, _ in u.launches]
+        i = kinds.index("gemm_wgrad")
+        assert kinds[i + 1] == "comm_allreduce_dw"
+        assert u.outputs[-1].dtype == torch.float32
+    assert sum(k.startswith("gemm") for u in units for k, _, _ in u.launches) == 12
