@@ -20,6 +20,15 @@ namespace {
 
 // Bit 0: a kernel gave up on a bounded wait.
 __device__ unsigned int g_status_word;
+// Where fp8bq_check's exchange kernel leaves the word it took.
+__device__ unsigned int g_status_taken;
+
+// Reads the status word and clears it in one atomic step, so a timeout that
+// a kernel on another stream records meanwhile is either taken now or stays
+// for the next check.
+__global__ void status_take_kernel(unsigned int* status, unsigned int* taken) {
+    *taken = atomicExch(status, 0u);
+}
 
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
 constexpr int kMaxDevices = 64;
@@ -30,6 +39,8 @@ struct DeviceState {
     int sms = 0;
     int max_pairs = 0;               // co-resident GEMM clusters (CTA pairs)
     unsigned int* status = nullptr;  // device address of g_status_word
+    unsigned int* taken = nullptr;   // device address of g_status_taken
+    std::mutex check_mu;             // one fp8bq_check at a time uses `taken`
 };
 
 // Launch configuration of the GEMM: `pairs` clusters of two CTAs.
@@ -69,7 +80,7 @@ cudaError_t set_tile_smem() {
     return e;
 }
 
-int probe_device(DeviceState** out) {
+fp8bq_status probe_device(DeviceState** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return FP8BQ_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return FP8BQ_ERR_DEVICE;
@@ -87,6 +98,8 @@ int probe_device(DeviceState** out) {
             void* p = nullptr;
             if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return FP8BQ_ERR_CUDA;
             d.status = static_cast<unsigned int*>(p);
+            if (cudaGetSymbolAddress(&p, g_status_taken) != cudaSuccess) return FP8BQ_ERR_CUDA;
+            d.taken = static_cast<unsigned int*>(p);
             const int smem = static_cast<int>(fp8bq::kGemmSmemBytes);
             if (cudaFuncSetAttribute(fp8bq::gemm_block_scaled_kernel<fp8bq::kModeFprop>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
@@ -135,13 +148,61 @@ int probe_device(DeviceState** out) {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Encoded TMA descriptors of recent calls.  A descriptor depends only on the
+// arguments of the encode call (address, extents, box, element type,
+// swizzle), which together form the key, so a hit is exactly the descriptor
+// the encode would produce; repeated calls on the same buffers (every step of
+// a training loop) skip the driver's encode.  Round-robin replacement.
+struct MapKey {
+    const void* ptr;
+    uint64_t inner, outer;
+    uint32_t box_inner, box_outer;
+    int kind;
+    bool operator==(const MapKey& o) const {
+        return ptr == o.ptr && inner == o.inner && outer == o.outer && box_inner == o.box_inner &&
+               box_outer == o.box_outer && kind == o.kind;
+    }
+};
+
+class MapCache {
+   public:
+    template <typename Encode>
+    fp8bq_status get(const MapKey& k, CUtensorMap* out, Encode encode) {
+        {
+            std::lock_guard<std::mutex> lock(mu_);
+            for (int i = 0; i < n_; ++i)
+                if (keys_[i] == k) {
+                    *out = maps_[i];
+                    return FP8BQ_OK;
+                }
+        }
+        const fp8bq_status st = encode(out);
+        if (st != FP8BQ_OK) return st;
+        std::lock_guard<std::mutex> lock(mu_);
+        const int i = n_ < kSize ? n_++ : next_;
+        next_ = (i + 1) % kSize;
+        keys_[i] = k;
+        maps_[i] = *out;
+        return FP8BQ_OK;
+    }
+
+   private:
+    static constexpr int kSize = 64;
+    std::mutex mu_;
+    MapKey keys_[kSize];
+    CUtensorMap maps_[kSize];
+    int n_ = 0, next_ = 0;
+};
+
+MapCache g_maps;
+
 inline int elem_size(int dtype) { return dtype == FP8BQ_BF16 ? 2 : 4; }
 
-inline int launch_status() { return cudaGetLastError() == cudaSuccess ? FP8BQ_OK : FP8BQ_ERR_CUDA; }
+inline fp8bq_status launch_status() { return cudaGetLastError() == cudaSuccess ? FP8BQ_OK : FP8BQ_ERR_CUDA; }
 
 // 2-D uint8 tensor [outer][inner] (inner contiguous, pitch == inner), tiles of
 // box_outer x 128 bytes with 128-byte swizzle.  Rows past `outer` read as 0.
-int encode_u8_map(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+fp8bq_status encode_u8_map_uncached(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_outer) {
     const cuuint64_t dims[2] = {inner, outer};
     const cuuint64_t strides[1] = {inner};
     const cuuint32_t box[2] = {128, box_outer};
@@ -152,10 +213,16 @@ int encode_u8_map(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t ou
     return r == CUDA_SUCCESS ? FP8BQ_OK : FP8BQ_ERR_CUDA;
 }
 
+fp8bq_status encode_u8_map(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+    return g_maps.get(MapKey{ptr, inner, outer, 128, box_outer, 0}, map, [&](CUtensorMap* m) {
+        return encode_u8_map_uncached(m, ptr, inner, outer, box_outer);
+    });
+}
+
 // 2-D output [rows][cols] (dense), BF16 or FP32, store boxes of 32 rows x
 // 64 bytes (32 BF16 or 16 FP32 columns) with 64-byte swizzle, matching the
 // epilogue staging.
-int encode_out_map(CUtensorMap* map, void* ptr, uint64_t cols, uint64_t rows, bool f32) {
+fp8bq_status encode_out_map_uncached(CUtensorMap* map, void* ptr, uint64_t cols, uint64_t rows, bool f32) {
     const cuuint64_t dims[2] = {cols, rows};
     const cuuint64_t strides[1] = {cols * (f32 ? 4 : 2)};
     const cuuint32_t box[2] = {f32 ? 16u : 32u, 32};
@@ -166,9 +233,15 @@ int encode_out_map(CUtensorMap* map, void* ptr, uint64_t cols, uint64_t rows, bo
     return r == CUDA_SUCCESS ? FP8BQ_OK : FP8BQ_ERR_CUDA;
 }
 
+fp8bq_status encode_out_map(CUtensorMap* map, void* ptr, uint64_t cols, uint64_t rows, bool f32) {
+    return g_maps.get(MapKey{ptr, cols, rows, f32 ? 16u : 32u, 32, f32 ? 2 : 1}, map, [&](CUtensorMap* m) {
+        return encode_out_map_uncached(m, ptr, cols, rows, f32);
+    });
+}
+
 // One 128x128 slab per CTA: grid (ceil(C/128), R/128).
 template <int kMode>
-int launch_tile(const void* x, int dtype, int64_t R, int64_t C, int64_t ldx, uint8_t* q, float* s_row, uint8_t* qT,
+fp8bq_status launch_tile(const void* x, int dtype, int64_t R, int64_t C, int64_t ldx, uint8_t* q, float* s_row, uint8_t* qT,
                 float* s_col, cudaStream_t cs) {
     dim3 grid(static_cast<unsigned>((C + 127) / 128), static_cast<unsigned>(R / 128));
     if (dtype == FP8BQ_BF16)
@@ -200,7 +273,7 @@ __global__ void fill_f32_kernel(float* p, int64_t n, float v) {
 
 // 2-D uint8 output [rows][cols] (dense), store boxes of 32 rows x 64 bytes
 // with 64-byte swizzle (the quantized-output epilogue's staging).
-int encode_u8_out_map(CUtensorMap* map, void* ptr, uint64_t cols, uint64_t rows) {
+fp8bq_status encode_u8_out_map_uncached(CUtensorMap* map, void* ptr, uint64_t cols, uint64_t rows) {
     const cuuint64_t dims[2] = {cols, rows};
     const cuuint64_t strides[1] = {cols};
     const cuuint32_t box[2] = {64, 32};
@@ -211,10 +284,16 @@ int encode_u8_out_map(CUtensorMap* map, void* ptr, uint64_t cols, uint64_t rows)
     return r == CUDA_SUCCESS ? FP8BQ_OK : FP8BQ_ERR_CUDA;
 }
 
+fp8bq_status encode_u8_out_map(CUtensorMap* map, void* ptr, uint64_t cols, uint64_t rows) {
+    return g_maps.get(MapKey{ptr, cols, rows, 64, 32, 3}, map, [&](CUtensorMap* m) {
+        return encode_u8_out_map_uncached(m, ptr, cols, rows);
+    });
+}
+
 // One 128x128 slab per CTA: grid (C/128, M/128).  Column-wise codes always,
 // row-wise codes too when kRows.
 template <bool kRows>
-int launch_mx_slab(const void* x, int dtype, int64_t M, int64_t C, int64_t ldx, uint8_t* qT, uint8_t* e8T,
+fp8bq_status launch_mx_slab(const void* x, int dtype, int64_t M, int64_t C, int64_t ldx, uint8_t* qT, uint8_t* e8T,
                    uint8_t* q, uint8_t* e8, cudaStream_t cs) {
     dim3 grid(static_cast<unsigned>(C / 128), static_cast<unsigned>(M / 128));
     uint16_t* ehT = reinterpret_cast<uint16_t*>(e8T);
@@ -229,7 +308,7 @@ int launch_mx_slab(const void* x, int dtype, int64_t M, int64_t C, int64_t ldx, 
 }
 
 template <int MODE>
-int run_gemm(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, const GemmOut& o, int64_t I,
+fp8bq_status run_gemm(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB, const GemmOut& o, int64_t I,
              int64_t J, int64_t Kr, cudaStream_t stream) {
     if (I < 0 || J < 0 || Kr < 0) return FP8BQ_ERR_SHAPE;
     if ((I % 128) || (J % 128) || (Kr % 128)) return FP8BQ_ERR_SHAPE;
@@ -241,7 +320,7 @@ int run_gemm(const uint8_t* A, const float* sA, const uint8_t* B, const float* s
     if ((o.d && !aligned16(o.d)) || (o.q && (!aligned16(o.q) || !aligned16(o.sq)))) return FP8BQ_ERR_ALIGN;
     if (Kr > 0 && (!aligned16(A) || !aligned16(B) || !aligned16(sA) || !aligned16(sB))) return FP8BQ_ERR_ALIGN;
     DeviceState* dev = nullptr;
-    int st = probe_device(&dev);
+    fp8bq_status st = probe_device(&dev);
     if (st != FP8BQ_OK) return st;
     if (Kr == 0) {
         // empty reduction: the product is exactly zero (adding it changes
@@ -260,7 +339,7 @@ int run_gemm(const uint8_t* A, const float* sA, const uint8_t* B, const float* s
 
     CUtensorMap ta, tb, td, tq;
     if (encode_u8_map(&ta, A, Kr, I, fp8bq::kBM) != FP8BQ_OK) return FP8BQ_ERR_CUDA;
-    if (encode_u8_map(&tb, B, Kr, J, fp8bq::kBNHalf) != FP8BQ_OK) return FP8BQ_ERR_CUDA;
+    if (encode_u8_map(&tb, B, Kr, J, fp8bq::kBRows) != FP8BQ_OK) return FP8BQ_ERR_CUDA;
     if (o.d && encode_out_map(&td, o.d, J, I, o.f32) != FP8BQ_OK) return FP8BQ_ERR_CUDA;
     if (o.q && encode_u8_out_map(&tq, o.q, J, I) != FP8BQ_OK) return FP8BQ_ERR_CUDA;
     if (!o.d) td = tq;  // unused by the kernel
@@ -297,15 +376,15 @@ int run_gemm(const uint8_t* A, const float* sA, const uint8_t* B, const float* s
 
 extern "C" {
 
-int fp8bq_quantize_rowwise(const void* x, int dtype, int64_t R, int64_t C, int64_t ldx, uint8_t* q, float* s,
-                           fp8bq_stream_t stream) {
+fp8bq_status fp8bq_quantize_rowwise(const void* x, fp8bq_dtype dtype, int64_t R, int64_t C, int64_t ldx, uint8_t* q, float* s,
+                                    fp8bq_stream_t stream) {
     if (dtype != FP8BQ_BF16 && dtype != FP8BQ_F32) return FP8BQ_ERR_DTYPE;
     if (R < 0 || C < 0 || ldx < C || (C % 128)) return FP8BQ_ERR_SHAPE;
     if (R == 0 || C == 0) return FP8BQ_OK;
     if (!x || !q || !s) return FP8BQ_ERR_NULL;
     if (!aligned16(x) || !aligned16(q) || !aligned16(s) || ((ldx * elem_size(dtype)) % 16)) return FP8BQ_ERR_ALIGN;
     DeviceState* dev = nullptr;
-    int st = probe_device(&dev);
+    fp8bq_status st = probe_device(&dev);
     if (st != FP8BQ_OK) return st;
     const int64_t tiles = R * (C / 128);
     if (tiles >= (int64_t(1) << 31)) return FP8BQ_ERR_SHAPE;  // the kernel indexes tiles in 32 bits
@@ -318,8 +397,8 @@ int fp8bq_quantize_rowwise(const void* x, int dtype, int64_t R, int64_t C, int64
     return launch_status();
 }
 
-int fp8bq_quantize_colwise(const void* x, int dtype, int64_t M, int64_t C, int64_t ldx, uint8_t* qT, float* s,
-                           fp8bq_stream_t stream) {
+fp8bq_status fp8bq_quantize_colwise(const void* x, fp8bq_dtype dtype, int64_t M, int64_t C, int64_t ldx, uint8_t* qT, float* s,
+                                    fp8bq_stream_t stream) {
     if (dtype != FP8BQ_BF16 && dtype != FP8BQ_F32) return FP8BQ_ERR_DTYPE;
     if (M < 0 || C < 0 || ldx < C || (M % 128) || (C % 8)) return FP8BQ_ERR_SHAPE;
     if (M == 0 || C == 0) return FP8BQ_OK;
@@ -327,14 +406,14 @@ int fp8bq_quantize_colwise(const void* x, int dtype, int64_t M, int64_t C, int64
     if (!aligned16(x) || !aligned16(qT) || !aligned16(s) || ((ldx * elem_size(dtype)) % 16)) return FP8BQ_ERR_ALIGN;
     if (M / 128 > 65535 || (C + 127) / 128 >= (int64_t(1) << 31)) return FP8BQ_ERR_SHAPE;
     DeviceState* dev = nullptr;
-    int st = probe_device(&dev);
+    fp8bq_status st = probe_device(&dev);
     if (st != FP8BQ_OK) return st;
     return launch_tile<fp8bq::kTileCol>(x, dtype, M, C, ldx, nullptr, nullptr, qT, s,
                                         reinterpret_cast<cudaStream_t>(stream));
 }
 
-int fp8bq_quantize_rowcol(const void* x, int dtype, int64_t M, int64_t C, int64_t ldx, uint8_t* q, float* s_row,
-                          uint8_t* qT, float* s_col, fp8bq_stream_t stream) {
+fp8bq_status fp8bq_quantize_rowcol(const void* x, fp8bq_dtype dtype, int64_t M, int64_t C, int64_t ldx, uint8_t* q, float* s_row,
+                                   uint8_t* qT, float* s_col, fp8bq_stream_t stream) {
     if (dtype != FP8BQ_BF16 && dtype != FP8BQ_F32) return FP8BQ_ERR_DTYPE;
     if (M < 0 || C < 0 || ldx < C || (M % 128) || (C % 128)) return FP8BQ_ERR_SHAPE;
     if (M == 0 || C == 0) return FP8BQ_OK;
@@ -344,14 +423,14 @@ int fp8bq_quantize_rowcol(const void* x, int dtype, int64_t M, int64_t C, int64_
         return FP8BQ_ERR_ALIGN;
     if (M / 128 > 65535 || C / 128 >= (int64_t(1) << 31)) return FP8BQ_ERR_SHAPE;
     DeviceState* dev = nullptr;
-    int st = probe_device(&dev);
+    fp8bq_status st = probe_device(&dev);
     if (st != FP8BQ_OK) return st;
     return launch_tile<fp8bq::kTileDual>(x, dtype, M, C, ldx, q, s_row, qT, s_col,
                                          reinterpret_cast<cudaStream_t>(stream));
 }
 
-int fp8bq_swiglu_quantize(const void* gu, int64_t M, int64_t F, int64_t ldgu, uint16_t* h, uint8_t* q,
-                          float* s_row, uint8_t* qT, float* s_col, fp8bq_stream_t stream) {
+fp8bq_status fp8bq_swiglu_quantize(const void* gu, int64_t M, int64_t F, int64_t ldgu, uint16_t* h, uint8_t* q,
+                                   float* s_row, uint8_t* qT, float* s_col, fp8bq_stream_t stream) {
     if (M < 0 || F < 0 || (M % 128) || (F % 128) || ldgu < 2 * F) return FP8BQ_ERR_SHAPE;
     if (M == 0 || F == 0) return FP8BQ_OK;
     if (!gu || !q || !s_row || !qT || !s_col) return FP8BQ_ERR_NULL;
@@ -360,7 +439,7 @@ int fp8bq_swiglu_quantize(const void* gu, int64_t M, int64_t F, int64_t ldgu, ui
         return FP8BQ_ERR_ALIGN;
     if (M / 128 > 65535 || F / 128 >= (int64_t(1) << 31)) return FP8BQ_ERR_SHAPE;
     DeviceState* dev = nullptr;
-    int st = probe_device(&dev);
+    fp8bq_status st = probe_device(&dev);
     if (st != FP8BQ_OK) return st;
     dim3 grid(static_cast<unsigned>(F / 128), static_cast<unsigned>(M / 128));
     fp8bq::quantize_tile_kernel<false, fp8bq::kTileSwiglu>
@@ -369,8 +448,8 @@ int fp8bq_swiglu_quantize(const void* gu, int64_t M, int64_t F, int64_t ldgu, ui
     return launch_status();
 }
 
-int fp8bq_quantize_weight_block(const void* w, int dtype, int64_t N, int64_t K, int64_t ldw, uint8_t* q,
-                                uint8_t* qT, float* s, fp8bq_stream_t stream) {
+fp8bq_status fp8bq_quantize_weight_block(const void* w, fp8bq_dtype dtype, int64_t N, int64_t K, int64_t ldw, uint8_t* q,
+                                         uint8_t* qT, float* s, fp8bq_stream_t stream) {
     if (dtype != FP8BQ_BF16 && dtype != FP8BQ_F32) return FP8BQ_ERR_DTYPE;
     if (N < 0 || K < 0 || ldw < K || (N % 128) || (K % 128)) return FP8BQ_ERR_SHAPE;
     if (N == 0 || K == 0) return FP8BQ_OK;
@@ -380,22 +459,22 @@ int fp8bq_quantize_weight_block(const void* w, int dtype, int64_t N, int64_t K, 
         return FP8BQ_ERR_ALIGN;
     if (N / 128 > 65535 || K / 128 >= (int64_t(1) << 31)) return FP8BQ_ERR_SHAPE;
     DeviceState* dev = nullptr;
-    int st = probe_device(&dev);
+    fp8bq_status st = probe_device(&dev);
     if (st != FP8BQ_OK) return st;
     return launch_tile<fp8bq::kTileWeight>(w, dtype, N, K, ldw, q, s, qT, nullptr,
                                            reinterpret_cast<cudaStream_t>(stream));
 }
 
-int fp8bq_gemm_fprop(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw, uint16_t* y, int64_t M,
-                     int64_t N, int64_t K, fp8bq_stream_t stream) {
+fp8bq_status fp8bq_gemm_fprop(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw, uint16_t* y, int64_t M,
+                              int64_t N, int64_t K, fp8bq_stream_t stream) {
     if (y == nullptr && M > 0 && N > 0) return FP8BQ_ERR_NULL;
     GemmOut o;
     o.d = y;
     return run_gemm<fp8bq::kModeFprop>(xq, sx, wq, sw, o, M, N, K, reinterpret_cast<cudaStream_t>(stream));
 }
 
-int fp8bq_gemm_fprop_q(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw, uint16_t* y,
-                       uint8_t* yq, float* sy, int64_t M, int64_t N, int64_t K, fp8bq_stream_t stream) {
+fp8bq_status fp8bq_gemm_fprop_q(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw, uint16_t* y,
+                                uint8_t* yq, float* sy, int64_t M, int64_t N, int64_t K, fp8bq_stream_t stream) {
     if ((yq == nullptr || sy == nullptr) && M > 0 && N > 0) return FP8BQ_ERR_NULL;
     GemmOut o;
     o.d = y;
@@ -404,24 +483,24 @@ int fp8bq_gemm_fprop_q(const uint8_t* xq, const float* sx, const uint8_t* wq, co
     return run_gemm<fp8bq::kModeFprop>(xq, sx, wq, sw, o, M, N, K, reinterpret_cast<cudaStream_t>(stream));
 }
 
-int fp8bq_gemm_dgrad(const uint8_t* dyq, const float* sdy, const uint8_t* wqT, const float* sw, uint16_t* dx,
-                     int64_t M, int64_t N, int64_t K, fp8bq_stream_t stream) {
+fp8bq_status fp8bq_gemm_dgrad(const uint8_t* dyq, const float* sdy, const uint8_t* wqT, const float* sw, uint16_t* dx,
+                              int64_t M, int64_t N, int64_t K, fp8bq_stream_t stream) {
     if (dx == nullptr && M > 0 && K > 0) return FP8BQ_ERR_NULL;
     GemmOut o;
     o.d = dx;
     return run_gemm<fp8bq::kModeDgrad>(dyq, sdy, wqT, sw, o, M, K, N, reinterpret_cast<cudaStream_t>(stream));
 }
 
-int fp8bq_gemm_wgrad(const uint8_t* dyqT, const float* sdyT, const uint8_t* xqT, const float* sxT, uint16_t* dw,
-                     int64_t M, int64_t N, int64_t K, fp8bq_stream_t stream) {
+fp8bq_status fp8bq_gemm_wgrad(const uint8_t* dyqT, const float* sdyT, const uint8_t* xqT, const float* sxT, uint16_t* dw,
+                              int64_t M, int64_t N, int64_t K, fp8bq_stream_t stream) {
     if (dw == nullptr && N > 0 && K > 0) return FP8BQ_ERR_NULL;
     GemmOut o;
     o.d = dw;
     return run_gemm<fp8bq::kModeWgrad>(dyqT, sdyT, xqT, sxT, o, N, K, M, reinterpret_cast<cudaStream_t>(stream));
 }
 
-int fp8bq_gemm_wgrad_f32(const uint8_t* dyqT, const float* sdyT, const uint8_t* xqT, const float* sxT, float* dw,
-                         int64_t M, int64_t N, int64_t K, int accumulate, fp8bq_stream_t stream) {
+fp8bq_status fp8bq_gemm_wgrad_f32(const uint8_t* dyqT, const float* sdyT, const uint8_t* xqT, const float* sxT, float* dw,
+                                  int64_t M, int64_t N, int64_t K, int accumulate, fp8bq_stream_t stream) {
     if (accumulate != 0 && accumulate != 1) return FP8BQ_ERR_SHAPE;
     if (dw == nullptr && N > 0 && K > 0) return FP8BQ_ERR_NULL;
     GemmOut o;
@@ -431,8 +510,8 @@ int fp8bq_gemm_wgrad_f32(const uint8_t* dyqT, const float* sdyT, const uint8_t* 
     return run_gemm<fp8bq::kModeWgrad>(dyqT, sdyT, xqT, sxT, o, N, K, M, reinterpret_cast<cudaStream_t>(stream));
 }
 
-int fp8bq_mx_quantize_rowwise(const void* x, int dtype, int64_t R, int64_t C, int64_t ldx, uint8_t* q,
-                              uint8_t* e8, fp8bq_stream_t stream) {
+fp8bq_status fp8bq_mx_quantize_rowwise(const void* x, fp8bq_dtype dtype, int64_t R, int64_t C, int64_t ldx, uint8_t* q,
+                                       uint8_t* e8, fp8bq_stream_t stream) {
     if (dtype != FP8BQ_BF16 && dtype != FP8BQ_F32) return FP8BQ_ERR_DTYPE;
     if (R < 0 || C < 0 || ldx < C || (C % 128)) return FP8BQ_ERR_SHAPE;
     if (R == 0 || C == 0) return FP8BQ_OK;
@@ -441,7 +520,7 @@ int fp8bq_mx_quantize_rowwise(const void* x, int dtype, int64_t R, int64_t C, in
     const int64_t nb = R * (C / 32);
     if (nb >= (int64_t(1) << 31)) return FP8BQ_ERR_SHAPE;  // the kernel numbers blocks in 32 bits
     DeviceState* dev = nullptr;
-    int st = probe_device(&dev);
+    fp8bq_status st = probe_device(&dev);
     if (st != FP8BQ_OK) return st;
     const int64_t per_warp = (dtype == FP8BQ_BF16 ? 8 : 4) * fp8bq::kMxRowSteps;
     const int64_t blocks = ((nb + per_warp - 1) / per_warp + 7) / 8;
@@ -454,8 +533,8 @@ int fp8bq_mx_quantize_rowwise(const void* x, int dtype, int64_t R, int64_t C, in
     return launch_status();
 }
 
-int fp8bq_mx_quantize_colwise(const void* x, int dtype, int64_t M, int64_t C, int64_t ldx, uint8_t* qT,
-                              uint8_t* e8, fp8bq_stream_t stream) {
+fp8bq_status fp8bq_mx_quantize_colwise(const void* x, fp8bq_dtype dtype, int64_t M, int64_t C, int64_t ldx, uint8_t* qT,
+                                       uint8_t* e8, fp8bq_stream_t stream) {
     if (dtype != FP8BQ_BF16 && dtype != FP8BQ_F32) return FP8BQ_ERR_DTYPE;
     if (M < 0 || C < 0 || ldx < C || (M % 128) || (C % 128)) return FP8BQ_ERR_SHAPE;
     if (M == 0 || C == 0) return FP8BQ_OK;
@@ -463,14 +542,14 @@ int fp8bq_mx_quantize_colwise(const void* x, int dtype, int64_t M, int64_t C, in
     if (!aligned16(x) || !aligned16(qT) || !aligned16(e8) || ((ldx * elem_size(dtype)) % 16)) return FP8BQ_ERR_ALIGN;
     if (M / 128 > 65535 || C / 128 >= (int64_t(1) << 31)) return FP8BQ_ERR_SHAPE;
     DeviceState* dev = nullptr;
-    int st = probe_device(&dev);
+    fp8bq_status st = probe_device(&dev);
     if (st != FP8BQ_OK) return st;
     return launch_mx_slab<false>(x, dtype, M, C, ldx, qT, e8, nullptr, nullptr,
                                  reinterpret_cast<cudaStream_t>(stream));
 }
 
-int fp8bq_mx_quantize_rowcol(const void* x, int dtype, int64_t M, int64_t C, int64_t ldx, uint8_t* q,
-                             uint8_t* e8, uint8_t* qT, uint8_t* e8T, fp8bq_stream_t stream) {
+fp8bq_status fp8bq_mx_quantize_rowcol(const void* x, fp8bq_dtype dtype, int64_t M, int64_t C, int64_t ldx, uint8_t* q,
+                                      uint8_t* e8, uint8_t* qT, uint8_t* e8T, fp8bq_stream_t stream) {
     if (dtype != FP8BQ_BF16 && dtype != FP8BQ_F32) return FP8BQ_ERR_DTYPE;
     if (M < 0 || C < 0 || ldx < C || (M % 128) || (C % 128)) return FP8BQ_ERR_SHAPE;
     if (M == 0 || C == 0) return FP8BQ_OK;
@@ -480,13 +559,13 @@ int fp8bq_mx_quantize_rowcol(const void* x, int dtype, int64_t M, int64_t C, int
         return FP8BQ_ERR_ALIGN;
     if (M / 128 > 65535 || C / 128 >= (int64_t(1) << 31)) return FP8BQ_ERR_SHAPE;
     DeviceState* dev = nullptr;
-    int st = probe_device(&dev);
+    fp8bq_status st = probe_device(&dev);
     if (st != FP8BQ_OK) return st;
     return launch_mx_slab<true>(x, dtype, M, C, ldx, qT, e8T, q, e8, reinterpret_cast<cudaStream_t>(stream));
 }
 
-int fp8bq_mx_gemm(const uint8_t* a, const uint8_t* ea, const uint8_t* b, const uint8_t* eb, uint16_t* d, int64_t I,
-                  int64_t J, int64_t K, fp8bq_stream_t stream) {
+fp8bq_status fp8bq_mx_gemm(const uint8_t* a, const uint8_t* ea, const uint8_t* b, const uint8_t* eb, uint16_t* d, int64_t I,
+                           int64_t J, int64_t K, fp8bq_stream_t stream) {
     if (I < 0 || J < 0 || K < 0 || (I % 128) || (J % 128) || (K % 128)) return FP8BQ_ERR_SHAPE;
     if (I >= (int64_t(1) << 31) || J >= (int64_t(1) << 31) || K >= (int64_t(1) << 31)) return FP8BQ_ERR_SHAPE;
     if (I == 0 || J == 0) return FP8BQ_OK;
@@ -495,7 +574,7 @@ int fp8bq_mx_gemm(const uint8_t* a, const uint8_t* ea, const uint8_t* b, const u
     if (!aligned16(d)) return FP8BQ_ERR_ALIGN;
     if (K > 0 && (!aligned16(a) || !aligned16(ea) || !aligned16(b) || !aligned16(eb))) return FP8BQ_ERR_ALIGN;
     DeviceState* dev = nullptr;
-    int st = probe_device(&dev);
+    fp8bq_status st = probe_device(&dev);
     if (st != FP8BQ_OK) return st;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     if (K == 0) {  // empty reduction: exact zeros
@@ -521,21 +600,23 @@ int fp8bq_mx_gemm(const uint8_t* a, const uint8_t* ea, const uint8_t* b, const u
     return launch_status();
 }
 
-int fp8bq_check(fp8bq_stream_t stream) {
+fp8bq_status fp8bq_check(fp8bq_stream_t stream) {
     DeviceState* dev = nullptr;
-    int st = probe_device(&dev);
+    fp8bq_status st = probe_device(&dev);
     if (st != FP8BQ_OK) return st;
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     unsigned int word = 0;
     if (cudaStreamSynchronize(cs) != cudaSuccess) return FP8BQ_ERR_CUDA;
-    if (cudaMemcpyAsync(&word, dev->status, sizeof(word), cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+    std::lock_guard<std::mutex> lock(dev->check_mu);
+    status_take_kernel<<<1, 1, 0, cs>>>(dev->status, dev->taken);
+    if (cudaGetLastError() != cudaSuccess) return FP8BQ_ERR_CUDA;
+    if (cudaMemcpyAsync(&word, dev->taken, sizeof(word), cudaMemcpyDeviceToHost, cs) != cudaSuccess)
         return FP8BQ_ERR_CUDA;
-    if (cudaMemsetAsync(dev->status, 0, sizeof(word), cs) != cudaSuccess) return FP8BQ_ERR_CUDA;
     if (cudaStreamSynchronize(cs) != cudaSuccess) return FP8BQ_ERR_CUDA;
     return (word & 1u) ? FP8BQ_ERR_TIMEOUT : FP8BQ_OK;
 }
 
-const char* fp8bq_status_string(int status) {
+const char* fp8bq_status_string(fp8bq_status status) {
     switch (status) {
         case FP8BQ_OK: return "ok";
         case FP8BQ_ERR_NULL: return "null pointer argument";
@@ -549,9 +630,9 @@ const char* fp8bq_status_string(int status) {
     }
 }
 
-int fp8bq_selftest_wait_timeout(int64_t limit_ns, fp8bq_stream_t stream) {
+fp8bq_status fp8bq_selftest_wait_timeout(int64_t limit_ns, fp8bq_stream_t stream) {
     DeviceState* dev = nullptr;
-    int st = probe_device(&dev);
+    fp8bq_status st = probe_device(&dev);
     if (st != FP8BQ_OK) return st;
     if (limit_ns < 1000) limit_ns = 1000;
     if (limit_ns > 2000000000ll) limit_ns = 2000000000ll;

@@ -79,9 +79,13 @@ typedef enum {
  *   q      [R][C] E4M3 codes, dense
  *   s      [C/128][R] FP32 scales: s[t*R + r] belongs to x[r][128t .. 128t+127]
  * Requires C % 128 == 0.
+ * Source: Puro-2B technical report (lkr-homepage blog), section 2 "FP8": the
+ *   main linear layers' matmuls in FP8 with DeepSeek-V3's fine-grained block
+ *   quantization; 1x128 tiles, E4M3, amax/448 and RNE are this library's
+ *   reading of it (the report prints no formula).
  */
-int fp8bq_quantize_rowwise(const void* x, int dtype, int64_t R, int64_t C, int64_t ldx,
-                           uint8_t* q, float* s, fp8bq_stream_t stream);
+fp8bq_status fp8bq_quantize_rowwise(const void* x, fp8bq_dtype dtype, int64_t R, int64_t C, int64_t ldx,
+                                    uint8_t* q, float* s, fp8bq_stream_t stream);
 
 /*
  * Column-wise 128x1 quantization emitted transposed (Wgrad operands: dY and
@@ -90,9 +94,12 @@ int fp8bq_quantize_rowwise(const void* x, int dtype, int64_t R, int64_t C, int64
  *   qT     [C][M] E4M3 codes: qT[c*M + m] is the code of x[m][c], dense
  *   s      [M/128][C] FP32 scales: s[b*C + c] belongs to x[128b .. 128b+127][c]
  * Requires M % 128 == 0 and C % 8 == 0 (16-byte rows of BF16).
+ * Source: Puro-2B technical report (lkr-homepage blog), section 2 "FP8" (as
+ *   fp8bq_quantize_rowwise), tiles along the token dimension that Wgrad
+ *   reduces over.
  */
-int fp8bq_quantize_colwise(const void* x, int dtype, int64_t M, int64_t C, int64_t ldx,
-                           uint8_t* qT, float* s, fp8bq_stream_t stream);
+fp8bq_status fp8bq_quantize_colwise(const void* x, fp8bq_dtype dtype, int64_t M, int64_t C, int64_t ldx,
+                                    uint8_t* qT, float* s, fp8bq_stream_t stream);
 
 /*
  * Row-wise 1x128 and column-wise 128x1 quantization of the same tensor in one
@@ -105,9 +112,11 @@ int fp8bq_quantize_colwise(const void* x, int dtype, int64_t M, int64_t C, int64
  *   q      [M][C] row-wise codes,      s_row [C/128][M]
  *   qT     [C][M] column-wise codes,   s_col [M/128][C]
  * Requires M % 128 == 0 and C % 128 == 0.
+ * Source: Puro-2B technical report (lkr-homepage blog), section 2 "FP8" (as
+ *   the two quantizers it fuses).
  */
-int fp8bq_quantize_rowcol(const void* x, int dtype, int64_t M, int64_t C, int64_t ldx,
-                          uint8_t* q, float* s_row, uint8_t* qT, float* s_col, fp8bq_stream_t stream);
+fp8bq_status fp8bq_quantize_rowcol(const void* x, fp8bq_dtype dtype, int64_t M, int64_t C, int64_t ldx,
+                                   uint8_t* q, float* s_row, uint8_t* qT, float* s_col, fp8bq_stream_t stream);
 
 /*
  * SwiGLU gate fused into the quantizer of the down projection's input.  From
@@ -126,9 +135,12 @@ int fp8bq_quantize_rowcol(const void* x, int dtype, int64_t M, int64_t C, int64_
  * and row pitch.  expf is the CUDA library's, so H may differ from a
  * correctly rounded silu(g) u by one BF16 ulp; the codes and scales are
  * always exactly those of the H the kernel formed.
+ * Source: Puro-2B technical report (lkr-homepage blog), section 2 "FP8" for
+ *   the quantization; the SwiGLU MLP of the 3.8B architecture in the n1n.ai
+ *   "$998 3.8B" article, model-architecture list, for the gate.
  */
-int fp8bq_swiglu_quantize(const void* gu, int64_t M, int64_t F, int64_t ldgu, uint16_t* h, uint8_t* q,
-                          float* s_row, uint8_t* qT, float* s_col, fp8bq_stream_t stream);
+fp8bq_status fp8bq_swiglu_quantize(const void* gu, int64_t M, int64_t F, int64_t ldgu, uint16_t* h, uint8_t* q,
+                                   float* s_row, uint8_t* qT, float* s_col, fp8bq_stream_t stream);
 
 /*
  * Weight quantization per 128x128 block.
@@ -137,9 +149,12 @@ int fp8bq_swiglu_quantize(const void* gu, int64_t M, int64_t F, int64_t ldgu, ui
  *   qT     [K][N] the same codes transposed (Dgrad operand), or NULL to skip
  *   s      [N/128][K/128] FP32 block scales
  * Requires N % 128 == 0 and K % 128 == 0.
+ * Source: Puro-2B technical report (lkr-homepage blog), section 2 "FP8":
+ *   fine-grained block quantization of the weights; 128x128 blocks are this
+ *   library's reading.
  */
-int fp8bq_quantize_weight_block(const void* w, int dtype, int64_t N, int64_t K, int64_t ldw,
-                                uint8_t* q, uint8_t* qT, float* s, fp8bq_stream_t stream);
+fp8bq_status fp8bq_quantize_weight_block(const void* w, fp8bq_dtype dtype, int64_t N, int64_t K, int64_t ldw,
+                                         uint8_t* q, uint8_t* qT, float* s, fp8bq_stream_t stream);
 
 /*
  * Fprop: Y[m][n] = sum_c sx[c][m] * sw[n/128][c] * sum_{k in chunk c} D(xq[m][k]) D(wq[n][k])
@@ -147,9 +162,12 @@ int fp8bq_quantize_weight_block(const void* w, int dtype, int64_t N, int64_t K, 
  *   wq [N][K] codes, sw [N/128][K/128] (from fp8bq_quantize_weight_block of W)
  *   y  [M][N] BF16 output (16-bit patterns), dense
  * Requires M, N, K % 128 == 0.
+ * Source: Puro-2B technical report (lkr-homepage blog), section 2 "FP8": FP8
+ *   matmul of the main linear layers, per-chunk FP32 promotion and BF16 output
+ *   as this library reads the recipe.
  */
-int fp8bq_gemm_fprop(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw,
-                     uint16_t* y, int64_t M, int64_t N, int64_t K, fp8bq_stream_t stream);
+fp8bq_status fp8bq_gemm_fprop(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw,
+                              uint16_t* y, int64_t M, int64_t N, int64_t K, fp8bq_stream_t stream);
 
 /*
  * Fprop whose epilogue also quantizes its output for a following linear
@@ -163,10 +181,12 @@ int fp8bq_gemm_fprop(const uint8_t* xq, const float* sx, const uint8_t* wq, cons
  *   sy  [N/128][M] their FP32 scales
  * Other arguments as fp8bq_gemm_fprop.  With K == 0 the output is zero:
  * codes +0, scales 1.
+ * Source: Puro-2B technical report (lkr-homepage blog), section 2 "FP8"
+ *   (Fprop, with the next layer's quantization fused).
  */
-int fp8bq_gemm_fprop_q(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw,
-                       uint16_t* y, uint8_t* yq, float* sy, int64_t M, int64_t N, int64_t K,
-                       fp8bq_stream_t stream);
+fp8bq_status fp8bq_gemm_fprop_q(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw,
+                                uint16_t* y, uint8_t* yq, float* sy, int64_t M, int64_t N, int64_t K,
+                                fp8bq_stream_t stream);
 
 /*
  * Dgrad: dX[m][k] = sum_c sdy[c][m] * sw[c][k/128] * sum_{n in chunk c} D(dyq[m][n]) D(wq[n][k])
@@ -175,9 +195,11 @@ int fp8bq_gemm_fprop_q(const uint8_t* xq, const float* sx, const uint8_t* wq, co
  *   sw  [N/128][K/128] the weight's block scales
  *   dx  [M][K] BF16 output, dense
  * Requires M, N, K % 128 == 0.
+ * Source: Puro-2B technical report (lkr-homepage blog), section 2 "FP8": the
+ *   backward matmul of the same linear layers.
  */
-int fp8bq_gemm_dgrad(const uint8_t* dyq, const float* sdy, const uint8_t* wqT, const float* sw,
-                     uint16_t* dx, int64_t M, int64_t N, int64_t K, fp8bq_stream_t stream);
+fp8bq_status fp8bq_gemm_dgrad(const uint8_t* dyq, const float* sdy, const uint8_t* wqT, const float* sw,
+                              uint16_t* dx, int64_t M, int64_t N, int64_t K, fp8bq_stream_t stream);
 
 /*
  * Wgrad: dW[n][k] = sum_c sdyT[c][n] * sxT[c][k] * sum_{m in chunk c} D(dyqT[n][m]) D(xqT[k][m])
@@ -185,9 +207,11 @@ int fp8bq_gemm_dgrad(const uint8_t* dyq, const float* sdy, const uint8_t* wqT, c
  *   xqT  [K][M] codes, sxT  [M/128][K] (from fp8bq_quantize_colwise of X)
  *   dw   [N][K] BF16 output, dense
  * Requires M, N, K % 128 == 0.
+ * Source: Puro-2B technical report (lkr-homepage blog), section 2 "FP8": the
+ *   weight-gradient matmul of the same linear layers.
  */
-int fp8bq_gemm_wgrad(const uint8_t* dyqT, const float* sdyT, const uint8_t* xqT, const float* sxT,
-                     uint16_t* dw, int64_t M, int64_t N, int64_t K, fp8bq_stream_t stream);
+fp8bq_status fp8bq_gemm_wgrad(const uint8_t* dyqT, const float* sdyT, const uint8_t* xqT, const float* sxT,
+                              uint16_t* dw, int64_t M, int64_t N, int64_t K, fp8bq_stream_t stream);
 
 /*
  * Wgrad with an FP32 output, for keeping weight gradients in FP32 across
@@ -200,9 +224,11 @@ int fp8bq_gemm_wgrad(const uint8_t* dyqT, const float* sdyT, const uint8_t* xqT,
  * Requires M, N, K % 128 == 0 and accumulate in {0, 1} (else FP8BQ_ERR_SHAPE).
  * The adds of accumulate = 1 are atomic per element: calls that overlap in
  * time on the same dw still sum correctly, in an unspecified order.
+ * Source: Puro-2B technical report (lkr-homepage blog), section 2 "FP8":
+ *   training state kept in FP32.
  */
-int fp8bq_gemm_wgrad_f32(const uint8_t* dyqT, const float* sdyT, const uint8_t* xqT, const float* sxT,
-                         float* dw, int64_t M, int64_t N, int64_t K, int accumulate, fp8bq_stream_t stream);
+fp8bq_status fp8bq_gemm_wgrad_f32(const uint8_t* dyqT, const float* sdyT, const uint8_t* xqT, const float* sxT,
+                                  float* dw, int64_t M, int64_t N, int64_t K, int accumulate, fp8bq_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * MX variant: one power-of-two scale per 1x32 block
@@ -230,9 +256,12 @@ int fp8bq_gemm_wgrad_f32(const uint8_t* dyqT, const float* sdyT, const uint8_t* 
  *   e8  [C/128][R][4] uint8 exponents (E + 127)
  * Requires C % 128 == 0 and R * C / 32 < 2^31.  One read of x.
  * Fprop operands: X [M][K] and W [N][K]; Dgrad's left operand dY [M][N].
+ * Source: no passage of the pages: the MX variant follows the OCP
+ *   Microscaling formats specification (block of 32, E8M0 scale) for
+ *   comparison with the report's recipe.
  */
-int fp8bq_mx_quantize_rowwise(const void* x, int dtype, int64_t R, int64_t C, int64_t ldx, uint8_t* q,
-                              uint8_t* e8, fp8bq_stream_t stream);
+fp8bq_status fp8bq_mx_quantize_rowwise(const void* x, fp8bq_dtype dtype, int64_t R, int64_t C, int64_t ldx, uint8_t* q,
+                                       uint8_t* e8, fp8bq_stream_t stream);
 
 /*
  * Column-wise MX quantization (32x1 blocks along M), emitted transposed.
@@ -242,9 +271,10 @@ int fp8bq_mx_quantize_rowwise(const void* x, int dtype, int64_t R, int64_t C, in
  * Requires M % 128 == 0, C % 128 == 0, M / 128 <= 65535.
  * Dgrad's right operand (W [N][K] -> [K][N]) and both Wgrad operands
  * (dY [M][N] -> [N][M], X [M][K] -> [K][M]).
+ * Source: as fp8bq_mx_quantize_rowwise.
  */
-int fp8bq_mx_quantize_colwise(const void* x, int dtype, int64_t M, int64_t C, int64_t ldx, uint8_t* qT,
-                              uint8_t* e8, fp8bq_stream_t stream);
+fp8bq_status fp8bq_mx_quantize_colwise(const void* x, fp8bq_dtype dtype, int64_t M, int64_t C, int64_t ldx, uint8_t* qT,
+                                       uint8_t* e8, fp8bq_stream_t stream);
 
 /*
  * Row-wise and column-wise MX quantization from one read of x: the outputs
@@ -255,9 +285,10 @@ int fp8bq_mx_quantize_colwise(const void* x, int dtype, int64_t M, int64_t C, in
  *   qT   [C][M] codes,   e8T [M/128][C][4] exponents (32x1 blocks along M)
  * Requires M % 128 == 0, C % 128 == 0, M / 128 <= 65535.  One pass serves
  * X (Fprop and Wgrad), W (Fprop and Dgrad) and dY (Dgrad and Wgrad).
+ * Source: as fp8bq_mx_quantize_rowwise.
  */
-int fp8bq_mx_quantize_rowcol(const void* x, int dtype, int64_t M, int64_t C, int64_t ldx, uint8_t* q,
-                             uint8_t* e8, uint8_t* qT, uint8_t* e8T, fp8bq_stream_t stream);
+fp8bq_status fp8bq_mx_quantize_rowcol(const void* x, fp8bq_dtype dtype, int64_t M, int64_t C, int64_t ldx, uint8_t* q,
+                                      uint8_t* e8, uint8_t* qT, uint8_t* e8T, fp8bq_stream_t stream);
 
 /*
  * MX GEMM: d[i][j] = BF16( sum_k 2^(ea(i,k)-127) D(a[i][k]) * 2^(eb(j,k)-127) D(b[j][k]) )
@@ -270,20 +301,23 @@ int fp8bq_mx_quantize_rowcol(const void* x, int dtype, int64_t M, int64_t C, int
  * Wgrad: (colwise dY, colwise X), I = N, J = K, reduction M.
  * The products accumulate in FP32 in tensor memory; the acceptance bound of
  * the FP32-scale GEMMs applies.  Requires I, J, K % 128 == 0 and each < 2^31.
+ * Source: as fp8bq_mx_quantize_rowwise (the block-scaled MMA applies the
+ *   scales).
  */
-int fp8bq_mx_gemm(const uint8_t* a, const uint8_t* ea, const uint8_t* b, const uint8_t* eb, uint16_t* d,
-                  int64_t I, int64_t J, int64_t K, fp8bq_stream_t stream);
+fp8bq_status fp8bq_mx_gemm(const uint8_t* a, const uint8_t* ea, const uint8_t* b, const uint8_t* eb, uint16_t* d,
+                           int64_t I, int64_t J, int64_t K, fp8bq_stream_t stream);
 
 /*
  * Synchronize `stream`, then read and clear the current device's status word.
  * Returns FP8BQ_OK, FP8BQ_ERR_TIMEOUT if a kernel launched since the last
  * check gave up on a pipeline wait (its outputs are then undefined), or
  * FP8BQ_ERR_CUDA if the synchronization itself failed.
+ * Source: no passage of the pages (failure detection of the library itself).
  */
-int fp8bq_check(fp8bq_stream_t stream);
+fp8bq_status fp8bq_check(fp8bq_stream_t stream);
 
 /* Static, human-readable name of a status code. */
-const char* fp8bq_status_string(int status);
+const char* fp8bq_status_string(fp8bq_status status);
 
 /*
  * Self-test of the bounded-wait path: launches one CTA that waits on a
@@ -292,8 +326,9 @@ const char* fp8bq_status_string(int status);
  * FP8BQ_ERR_TIMEOUT in the status word, exactly as a stalled GEMM pipeline
  * would.  Lets a caller verify, without faulting or hanging the GPU, that
  * fp8bq_check reports device-side timeouts.  Returns the launch status.
+ * Source: no passage of the pages (failure detection of the library itself).
  */
-int fp8bq_selftest_wait_timeout(int64_t limit_ns, fp8bq_stream_t stream);
+fp8bq_status fp8bq_selftest_wait_timeout(int64_t limit_ns, fp8bq_stream_t stream);
 
 #ifdef __cplusplus
 }
