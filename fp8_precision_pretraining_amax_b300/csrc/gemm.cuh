@@ -70,6 +70,7 @@ constexpr int kBM = 128;          // tile rows per CTA (TMEM lanes)
 constexpr int kPairM = 256;       // tile rows per CTA pair
 constexpr int kBN = 256;          // tile columns (MMA N)
 constexpr int kBNHalf = 128;      // B rows each CTA loads
+constexpr int kBRows = kBNHalf;   // B box height of the tensor map (rows per CTA)
 constexpr int kBK = 128;          // one scale chunk of the reduction
 constexpr int kStages = 6;
 constexpr int kScaleSlots = 6;
