@@ -241,8 +241,9 @@ fp8bq_status encode_out_map(CUtensorMap* map, void* ptr, uint64_t cols, uint64_t
 
 // One 128x128 slab per CTA: grid (ceil(C/128), R/128).
 template <int kMode>
-fp8bq_status launch_tile(const void* x, int dtype, int64_t R, int64_t C, int64_t ldx, uint8_t* q, float* s_row, uint8_t* qT,
-                float* s_col, cudaStream_t cs) {
+fp8bq_status launch_tile(const DeviceState* dev, const void* x, int dtype, int64_t R, int64_t C, int64_t ldx,
+                         uint8_t* q, float* s_row, uint8_t* qT, float* s_col, cudaStream_t cs) {
+    (void)dev;
     dim3 grid(static_cast<unsigned>((C + 127) / 128), static_cast<unsigned>(R / 128));
     if (dtype == FP8BQ_BF16)
         fp8bq::quantize_tile_kernel<false, kMode>
@@ -408,7 +409,7 @@ fp8bq_status fp8bq_quantize_colwise(const void* x, fp8bq_dtype dtype, int64_t M,
     DeviceState* dev = nullptr;
     fp8bq_status st = probe_device(&dev);
     if (st != FP8BQ_OK) return st;
-    return launch_tile<fp8bq::kTileCol>(x, dtype, M, C, ldx, nullptr, nullptr, qT, s,
+    return launch_tile<fp8bq::kTileCol>(dev, x, dtype, M, C, ldx, nullptr, nullptr, qT, s,
                                         reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -425,7 +426,7 @@ fp8bq_status fp8bq_quantize_rowcol(const void* x, fp8bq_dtype dtype, int64_t M, 
     DeviceState* dev = nullptr;
     fp8bq_status st = probe_device(&dev);
     if (st != FP8BQ_OK) return st;
-    return launch_tile<fp8bq::kTileDual>(x, dtype, M, C, ldx, q, s_row, qT, s_col,
+    return launch_tile<fp8bq::kTileDual>(dev, x, dtype, M, C, ldx, q, s_row, qT, s_col,
                                          reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -461,7 +462,7 @@ fp8bq_status fp8bq_quantize_weight_block(const void* w, fp8bq_dtype dtype, int64
     DeviceState* dev = nullptr;
     fp8bq_status st = probe_device(&dev);
     if (st != FP8BQ_OK) return st;
-    return launch_tile<fp8bq::kTileWeight>(w, dtype, N, K, ldw, q, s, qT, nullptr,
+    return launch_tile<fp8bq::kTileWeight>(dev, w, dtype, N, K, ldw, q, s, qT, nullptr,
                                            reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -52,19 +52,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return done != 0;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete
+// sleeps in hardware until the phase completes or `hint_ns` pass, instead of
+// polling (polling warps take issue slots from the warps they wait for).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return done != 0;
+}
+
 // Wait until the phase with the given parity has completed.  Returns false
 // (without completing the wait) when `limit_ns` elapses or when another role
 // of the CTA has raised `abort_flag` (may be null: wait for the time limit
-// only).
+// only); both are checked at least every 20 us.
 __device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                              uint64_t limit_ns) {
     const uint32_t a = smem_addr(bar);
     if (mbar_try_wait(a, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-#pragma unroll 1
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(a, parity)) return true;
+        if (mbar_try_wait_sleep(a, parity, 20000)) return true;
         if (abort_flag != nullptr && *abort_flag) return false;
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
@@ -332,15 +345,6 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
-// Arrive on a barrier of this or the peer CTA and raise its expected
-// transaction count by `bytes` (the bytes of copies this thread is about to
-// issue with completion on that barrier).
-__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t cluster_addr, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_addr),
-                 "r"(bytes)
-                 : "memory");
-}
-
 __device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
@@ -379,26 +383,6 @@ __device__ __forceinline__ void mma_e4m3_pair(uint32_t d_tmem, uint64_t a_desc, 
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// One 128-deep K chunk of the CTA pair: four 256 x N x 32 steps, the first
-// overwriting D, the others accumulating.  a_desc / b_desc describe the
-// chunk's first 32 K values; each further step starts 32 bytes (2 descriptor
-// units) later inside the 128-byte swizzled rows.
-__device__ __forceinline__ void mma_e4m3_pair_chunk(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                                    uint32_t idesc) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "add.s64 a1, %1, 2;\n\tadd.s64 a2, %1, 4;\n\tadd.s64 a3, %1, 6;\n\t"
-        "add.s64 b1, %2, 2;\n\tadd.s64 b2, %2, 4;\n\tadd.s64 b3, %2, 6;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t"
-        "setp.eq.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], a1, b1, %3, p;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], a2, b2, %3, p;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], a3, b3, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(0)
         : "memory");
 }
 

@@ -146,6 +146,7 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
+
 // ------------------------------------------------------------------ row-wise
 //
 // Helpers for a 1x128 row tile held by 4 lanes (32 values each, lane j owning
@@ -283,7 +284,7 @@ __global__ void __launch_bounds__(256) quantize_rowwise_kernel(const void* __res
 enum TileMode : int { kTileCol = 0, kTileDual = 1, kTileWeight = 2, kTileSwiglu = 3 };
 
 template <bool kF32, int kMode = kTileDual>
-constexpr int tile_smem_bytes() { return 128 * 128 * (kF32 ? 4 : 2) * (kMode == kTileSwiglu ? 2 : 1); }
+__host__ __device__ constexpr int tile_smem_bytes() { return 128 * 128 * (kF32 ? 4 : 2) * (kMode == kTileSwiglu ? 2 : 1); }
 
 // h = silu(g) * u = g u / (1 + exp(-g)) in FP32 (expf, IEEE division and
 // product), rounded to BF16 once.
@@ -291,32 +292,24 @@ __device__ __forceinline__ float swiglu_f32(float g, float u) {
     return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
 }
 
+// Shared-memory scratch of one slab's processing (besides the slab itself).
+template <bool kF32>
+struct SlabScratch {
+    static constexpr int G = 256 / ((128 * (kF32 ? 4 : 2)) / 4);   // row groups of the column view
+    float red[G][128];
+    float cdiv[2][128];    // per column (or [.][0] for the block): s, nr
+    float wred[8];
+};
+
+// Issues the 16-byte cp.async copies of the slab at (r0, c0) into shared
+// memory at `sbase` (row pitch 128 elements; the u slab of the SwiGLU mode
+// right after the g slab).  Columns past C read as zero.
 template <bool kF32, int kMode>
-__global__ void __launch_bounds__(256, 4) quantize_tile_kernel(const void* __restrict__ x, int64_t R, int64_t C,
-                                                            int64_t ldx, uint8_t* __restrict__ q,
-                                                            float* __restrict__ s_row, uint8_t* __restrict__ qT,
-                                                            float* __restrict__ s_col, int64_t uoff = 0,
-                                                            uint16_t* __restrict__ h = nullptr) {
-    static_assert(kMode != kTileSwiglu || !kF32, "the SwiGLU mode takes BF16 input");
+__device__ __forceinline__ void slab_load(uint32_t sbase, const uint8_t* xb, int64_t r0, int64_t c0, int64_t C,
+                                          int64_t ldx, int64_t uoff, int tid) {
     constexpr int E = kF32 ? 4 : 2;
-    constexpr int RB = 128 * E;       // slab row pitch in shared memory (bytes)
-    constexpr int CPR = RB / 16;      // 16-byte chunks per row
-    constexpr int UPR = RB / 4;       // 4-byte units per row (column view)
-    constexpr int VEC = 4 / E;        // columns per unit
-    constexpr int G = 256 / UPR;      // row groups (column view)
-    constexpr int RPG = 128 / G;      // rows per group
-    extern __shared__ __align__(16) uint8_t slab[];
-    __shared__ float red[G][128];
-    __shared__ float cdiv[2][128];    // per column (or [.][0] for the block): s, nr
-    __shared__ float wred[8];
-
-    const int tid = threadIdx.x;
-    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128;
-    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 128;
-    const uint8_t* xb = static_cast<const uint8_t*>(x);
-
-    // ---- stage the slab
-    const uint32_t sbase = smem_addr(slab);
+    constexpr int RB = 128 * E;
+    constexpr int CPR = RB / 16;
 #pragma unroll
     for (int k = 0; k < (128 * CPR) / 256; ++k) {
         const int i = tid + 256 * k;
@@ -328,8 +321,27 @@ __global__ void __launch_bounds__(256, 4) quantize_tile_kernel(const void* __res
         if (kMode == kTileSwiglu)  // u slab right after the g slab
             cp_async_16(sbase + 128 * RB + row * RB + ch * 16, src + uoff * E, ok ? 16u : 0u);
     }
-    cp_async_wait_all();
-    __syncthreads();
+}
+
+// Quantizes the slab at (r0, c0), already in shared memory at `slab`, into
+// the outputs of mode kMode (see the list above).  Every thread of the
+// 256-thread CTA takes part; the slab may be overwritten once it returns and
+// the CTA has synchronized.
+template <bool kF32, int kMode>
+__device__ __forceinline__ void slab_process(uint8_t* __restrict__ slab, SlabScratch<kF32>& sc, int64_t r0, int64_t c0,
+                                             int64_t R, int64_t C, uint8_t* __restrict__ q, float* __restrict__ s_row,
+                                             uint8_t* __restrict__ qT, float* __restrict__ s_col,
+                                             uint16_t* __restrict__ h, int tid) {
+    constexpr int E = kF32 ? 4 : 2;
+    constexpr int RB = 128 * E;       // slab row pitch in shared memory (bytes)
+    constexpr int CPR = RB / 16;      // 16-byte chunks per row
+    constexpr int UPR = RB / 4;       // 4-byte units per row (column view)
+    constexpr int VEC = 4 / E;        // columns per unit
+    constexpr int G = 256 / UPR;      // row groups (column view)
+    constexpr int RPG = 128 / G;      // rows per group
+    float (&red)[G][128] = sc.red;
+    float (&cdiv)[2][128] = sc.cdiv;
+    float (&wred)[8] = sc.wred;
 
     if (kMode == kTileSwiglu) {
         // H = BF16(silu(g) * u), in place over the g slab (and to h)
@@ -361,7 +373,7 @@ __global__ void __launch_bounds__(256, 4) quantize_tile_kernel(const void* __res
     const int u = tid % UPR, g = tid / UPR;
     const uint8_t* colp = slab + g * RPG * RB + u * 4;
     constexpr int NCW = kF32 ? 1 : RPG;
-    uint32_t cw[NCW];
+    uint32_t cw[NCW] = {};
     auto colword = [&](int i) -> uint32_t {
         return kF32 ? *reinterpret_cast<const uint32_t*>(colp + i * RB) : cw[kF32 ? 0 : i];
     };
@@ -481,6 +493,24 @@ __global__ void __launch_bounds__(256, 4) quantize_tile_kernel(const void* __res
         }
         store_row_quarter<kF32>(q + (r0 + row) * C + c0, j, v, d, flip);
     }
+}
+
+template <bool kF32, int kMode>
+__global__ void __launch_bounds__(256, 4) quantize_tile_kernel(const void* __restrict__ x, int64_t R, int64_t C,
+                                                            int64_t ldx, uint8_t* __restrict__ q,
+                                                            float* __restrict__ s_row, uint8_t* __restrict__ qT,
+                                                            float* __restrict__ s_col, int64_t uoff = 0,
+                                                            uint16_t* __restrict__ h = nullptr) {
+    static_assert(kMode != kTileSwiglu || !kF32, "the SwiGLU mode takes BF16 input");
+    extern __shared__ __align__(16) uint8_t slab[];
+    __shared__ SlabScratch<kF32> sc;
+    const int tid = threadIdx.x;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 128;
+    slab_load<kF32, kMode>(smem_addr(slab), static_cast<const uint8_t*>(x), r0, c0, C, ldx, uoff, tid);
+    cp_async_wait_all();
+    __syncthreads();
+    slab_process<kF32, kMode>(slab, sc, r0, c0, R, C, q, s_row, qT, s_col, h, tid);
 }
 
 }  // namespace fp8bq
