@@ -118,8 +118,8 @@ struct alignas(16) GemmCtl {
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
-    uint32_t issued;           // loads this CTA's producer issued
-    uint32_t peer_issued;      // even CTA: loads the odd CTA's producer issued
+    uint32_t issued;           // stages this CTA's producer filled
+    uint32_t peer_issued;      // even CTA: stages the odd CTA's producer filled
     uint32_t scl_issued;       // scale slots this CTA's scale producer filled
     ScaleSlot scl[kScaleSlots];
 };
@@ -546,13 +546,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
 
     // Teardown.  Every role has stopped (all waits are bounded).  The odd CTA
-    // reports how many loads its producer issued; after an abort each CTA
+    // reports how many stages its producer filled; after an abort each CTA
     // waits (bounded) for the scale copies it issued, and the even CTA for
     // every operand copy either producer issued and for its own in-flight
     // MMAs, which read both CTAs' shared memory and write both CTAs' TMEM,
-    // before either CTA frees TMEM or exits.  Only the last ring-depth copies
-    // can still be in flight: a slot is refilled only after its previous
-    // contents were consumed.
+    // before either CTA frees TMEM or exits.  A stage that only one producer
+    // filled is first made completable: the bytes of the half that was never
+    // loaded are counted as done (and, if the even producer stopped first,
+    // the stage is armed for both halves).  The producers are at most a ring
+    // apart (the odd one refills a stage only after the MMA consumed it, which
+    // needed the even one's arming), and only the last ring-depth stages can
+    // still be in flight: a stage is refilled only after its previous contents
+    // were consumed.
     tc_fence_before();
     __syncthreads();
     if (!leader && threadIdx.x == 0) st_cluster_u32(mapa_shared(smem_addr(&ctl->peer_issued), 0), ctl->issued);
@@ -565,7 +570,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     if (leader && *abort_flag) {
         if (warp == 0 && lane == 0) {
-            const uint32_t n = ctl->issued > ctl->peer_issued ? ctl->issued : ctl->peer_issued;
+            const uint32_t a = ctl->issued, b = ctl->peer_issued;
+            for (uint32_t f = b; f < a; ++f)   // the odd half never loaded
+                mbar_complete_tx(&ctl->full[f % kStages], kStageBytesA + kStageBytesB);
+            for (uint32_t f = a; f < b; ++f) {  // only the odd half loaded
+                mbar_arrive_expect_tx(&ctl->full[f % kStages], 2 * (kStageBytesA + kStageBytesB));
+                mbar_complete_tx(&ctl->full[f % kStages], kStageBytesA + kStageBytesB);
+            }
+            const uint32_t n = a > b ? a : b;
             const uint32_t f0 = n > static_cast<uint32_t>(kStages) ? n - kStages : 0;
             for (uint32_t f = f0; f < n; ++f)
                 bounded_wait(&ctl->full[f % kStages], (f / kStages) & 1, nullptr, lim);
