@@ -330,16 +330,23 @@ def build_units(fp8bq, name, lins, dev, world, variant="fp32-scale"):
         raise SystemExit("the MX variant is benchmarked on the layer_3p8b workload only")
     units = []
     if name == "layer_3p8b":
-        for lin in lins:
-            L = (LinearMX if mx else LinearFP8)(lin.M, lin.K, lin.N, device=dev)
-            launches = (step_launches_mx if mx else step_launches)(fp8bq, L, lin)
+        layers = [(LinearMX if mx else LinearFP8)(lin.M, lin.K, lin.N, device=dev) for lin in lins]
+        if not mx:
+            # every weight of the layer in one launch (the step quantizes them
+            # all once, as after an optimizer update)
+            wl = [(lin.w, L.wq, L.wqT, L.sw) for L, lin in zip(layers, lins)]
+            units.append(Unit("weights", [("quant_weight", sum(weight_bytes(l.N, l.K) for l in lins),
+                                           lambda: fp8bq.fp8bq_quantize_weight_blocks(wl))],
+                              [lin.w for lin in lins], []))
+        for L, lin in zip(layers, lins):
+            launches = step_launches_mx(fp8bq, L, lin) if mx else step_launches(fp8bq, L, lin)[1:]
             dw = L.dw
             if world > 1 and mx:  # the MX variant has no FP32 Wgrad: its BF16 dW is summed
                 launches.append(("comm_allreduce_dw", 2 * L.N * L.K,
                                  lambda L=L: dist.all_reduce(L.dw, op=dist.ReduceOp.SUM)))
             elif world > 1:
                 dw = data_parallel_wgrad(fp8bq, L, launches, dist)
-            units.append(Unit(lin.name, launches, (lin.x, lin.w, lin.dy), (L.y, L.dx, dw)))
+            units.append(Unit(lin.name, launches, (lin.x, lin.w, lin.dy) if mx else (lin.x, lin.dy), (L.y, L.dx, dw)))
     elif name == "swiglu":
         gu_lin, down_lin = lins
         M, D, F = gu_lin.M, gu_lin.K, down_lin.K

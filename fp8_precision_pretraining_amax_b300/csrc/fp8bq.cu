@@ -73,6 +73,9 @@ cudaError_t set_tile_smem() {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(fp8bq::quantize_tile_kernel<kF32, fp8bq::kTileWeight>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(fp8bq::quantize_weight_group_kernel<kF32>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e == cudaSuccess && !kF32)
         e = cudaFuncSetAttribute(fp8bq::quantize_tile_kernel<false, fp8bq::kTileSwiglu>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -464,6 +467,74 @@ fp8bq_status fp8bq_quantize_weight_block(const void* w, fp8bq_dtype dtype, int64
     if (st != FP8BQ_OK) return st;
     return launch_tile<fp8bq::kTileWeight>(dev, w, dtype, N, K, ldw, q, s, qT, nullptr,
                                            reinterpret_cast<cudaStream_t>(stream));
+}
+
+// Host-side checks of one weight block quantization (those of
+// fp8bq_quantize_weight_block).
+fp8bq_status check_weight_args(const void* w, int64_t N, int64_t K, int64_t ldw, const uint8_t* q, const uint8_t* qT,
+                               const float* s, int dtype) {
+    if (N < 0 || K < 0 || ldw < K || (N % 128) || (K % 128)) return FP8BQ_ERR_SHAPE;
+    if (N == 0 || K == 0) return FP8BQ_OK;
+    if (!w || !q || !s) return FP8BQ_ERR_NULL;
+    if (!aligned16(w) || !aligned16(q) || !aligned16(s) || (qT && !aligned16(qT)) ||
+        ((ldw * elem_size(dtype)) % 16))
+        return FP8BQ_ERR_ALIGN;
+    if (N / 128 > 65535 || K / 128 >= (int64_t(1) << 31)) return FP8BQ_ERR_SHAPE;
+    if ((N / 128) * (K / 128) >= (int64_t(1) << 31)) return FP8BQ_ERR_SHAPE;  // blocks are numbered in 32 bits
+    return FP8BQ_OK;
+}
+
+fp8bq_status fp8bq_quantize_weight_blocks(const fp8bq_weight* weights, int count, fp8bq_dtype dtype,
+                                          fp8bq_stream_t stream) {
+    if (dtype != FP8BQ_BF16 && dtype != FP8BQ_F32) return FP8BQ_ERR_DTYPE;
+    if (count < 0) return FP8BQ_ERR_SHAPE;
+    if (count == 0) return FP8BQ_OK;
+    if (!weights) return FP8BQ_ERR_NULL;
+    bool any = false;
+    for (int i = 0; i < count; ++i) {
+        const fp8bq_weight& e = weights[i];
+        const fp8bq_status st = check_weight_args(e.w, e.N, e.K, e.ldw, e.q, e.qT, e.s, dtype);
+        if (st != FP8BQ_OK) return st;
+        any = any || (e.N > 0 && e.K > 0);
+    }
+    if (!any) return FP8BQ_OK;
+    DeviceState* dev = nullptr;
+    fp8bq_status st = probe_device(&dev);
+    if (st != FP8BQ_OK) return st;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    int i = 0;
+    while (i < count) {
+        fp8bq::WeightGroup g = {};
+        int64_t blocks = 0;
+        for (; i < count && g.n < fp8bq::kMaxWeightGroup; ++i) {
+            const fp8bq_weight& e = weights[i];
+            if (e.N == 0 || e.K == 0) continue;
+            const int64_t nb = (e.N / 128) * (e.K / 128);
+            if (blocks + nb >= (int64_t(1) << 31)) break;
+            const int k = g.n++;
+            g.first_block[k] = static_cast<int>(blocks);
+            g.nbx[k] = static_cast<int>(e.K / 128);
+            g.w[k] = e.w;
+            g.N[k] = e.N;
+            g.K[k] = e.K;
+            g.ldw[k] = e.ldw;
+            g.q[k] = e.q;
+            g.qT[k] = e.qT;
+            g.s[k] = e.s;
+            blocks += nb;
+        }
+        if (g.n == 0) continue;
+        g.first_block[g.n] = static_cast<int>(blocks);
+        if (dtype == FP8BQ_BF16)
+            fp8bq::quantize_weight_group_kernel<false>
+                <<<static_cast<unsigned>(blocks), 256, fp8bq::tile_smem_bytes<false>(), cs>>>(g);
+        else
+            fp8bq::quantize_weight_group_kernel<true>
+                <<<static_cast<unsigned>(blocks), 256, fp8bq::tile_smem_bytes<true>(), cs>>>(g);
+        st = launch_status();
+        if (st != FP8BQ_OK) return st;
+    }
+    return FP8BQ_OK;
 }
 
 fp8bq_status fp8bq_gemm_fprop(const uint8_t* xq, const float* sx, const uint8_t* wq, const float* sw, uint16_t* y, int64_t M,

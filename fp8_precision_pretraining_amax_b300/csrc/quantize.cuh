@@ -286,10 +286,15 @@ enum TileMode : int { kTileCol = 0, kTileDual = 1, kTileWeight = 2, kTileSwiglu 
 template <bool kF32, int kMode = kTileDual>
 __host__ __device__ constexpr int tile_smem_bytes() { return 128 * 128 * (kF32 ? 4 : 2) * (kMode == kTileSwiglu ? 2 : 1); }
 
-// h = silu(g) * u = g u / (1 + exp(-g)) in FP32 (expf, IEEE division and
-// product), rounded to BF16 once.
+// h = silu(g) * u = g u / (1 + exp(-g)) in FP32, rounded to BF16 once.  The
+// exponential is the hardware approximation (__expf, relative error below
+// 2e-5 for |g| <= 88) and the division a correctly rounded reciprocal times
+// g: together far inside half a BF16 ulp (2^-9), so the BF16 h is within one
+// ulp of the exact value.  exp(-g) beyond the FP32 range is +inf and gives
+// h = +-0; the reciprocal keeps the FP32-subnormal range of 1 + exp(-g)
+// (g between about -88.7 and -87.3) exact enough.
 __device__ __forceinline__ float swiglu_f32(float g, float u) {
-    return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+    return __fmul_rn(__fmul_rn(g, __frcp_rn(__fadd_rn(1.0f, __expf(-g)))), u);
 }
 
 // Shared-memory scratch of one slab's processing (besides the slab itself).
@@ -511,6 +516,41 @@ __global__ void __launch_bounds__(256, 4) quantize_tile_kernel(const void* __res
     cp_async_wait_all();
     __syncthreads();
     slab_process<kF32, kMode>(slab, sc, r0, c0, R, C, q, s_row, qT, s_col, h, tid);
+}
+
+// Several weights' 128x128 block quantization in one launch: block b of the
+// grid is block b - first_block[i] (row-major over that weight's blocks) of
+// weight i, first_block[i] <= b < first_block[i + 1].  One launch replaces a
+// launch per weight, whose short grids end in a partly idle wave each.
+constexpr int kMaxWeightGroup = 16;
+
+struct WeightGroup {
+    int n;
+    int first_block[kMaxWeightGroup + 1];
+    int nbx[kMaxWeightGroup];   // blocks per row of blocks (K / 128)
+    const void* w[kMaxWeightGroup];
+    int64_t N[kMaxWeightGroup], K[kMaxWeightGroup], ldw[kMaxWeightGroup];
+    uint8_t* q[kMaxWeightGroup];
+    uint8_t* qT[kMaxWeightGroup];
+    float* s[kMaxWeightGroup];
+};
+
+template <bool kF32>
+__global__ void __launch_bounds__(256, 4) quantize_weight_group_kernel(const __grid_constant__ WeightGroup g) {
+    extern __shared__ __align__(16) uint8_t slab[];
+    __shared__ SlabScratch<kF32> sc;
+    const int tid = threadIdx.x;
+    const int b = static_cast<int>(blockIdx.x);
+    int i = 0;
+    while (i + 1 < g.n && b >= g.first_block[i + 1]) ++i;
+    const int lb = b - g.first_block[i];
+    const int64_t r0 = static_cast<int64_t>(lb / g.nbx[i]) * 128;
+    const int64_t c0 = static_cast<int64_t>(lb % g.nbx[i]) * 128;
+    slab_load<kF32, kTileWeight>(smem_addr(slab), static_cast<const uint8_t*>(g.w[i]), r0, c0, g.K[i], g.ldw[i], 0,
+                                 tid);
+    cp_async_wait_all();
+    __syncthreads();
+    slab_process<kF32, kTileWeight>(slab, sc, r0, c0, g.N[i], g.K[i], g.q[i], g.s[i], g.qT[i], nullptr, nullptr, tid);
 }
 
 }  // namespace fp8bq

@@ -26,10 +26,16 @@ BF16, F32 = 0, 1
 #: Names of the C-ABI entry points declared in include/fp8bq.h.
 C_FUNCTIONS = (
     "fp8bq_quantize_rowwise", "fp8bq_quantize_colwise", "fp8bq_quantize_rowcol", "fp8bq_swiglu_quantize",
-    "fp8bq_quantize_weight_block", "fp8bq_gemm_fprop", "fp8bq_gemm_fprop_q", "fp8bq_gemm_dgrad",
+    "fp8bq_quantize_weight_block", "fp8bq_quantize_weight_blocks", "fp8bq_gemm_fprop", "fp8bq_gemm_fprop_q", "fp8bq_gemm_dgrad",
     "fp8bq_gemm_wgrad", "fp8bq_gemm_wgrad_f32", "fp8bq_mx_quantize_rowwise", "fp8bq_mx_quantize_colwise",
     "fp8bq_mx_quantize_rowcol", "fp8bq_mx_gemm", "fp8bq_check", "fp8bq_status_string", "fp8bq_selftest_wait_timeout",
 )
+
+
+class FP8BQWeight(ctypes.Structure):
+    """One entry of fp8bq_quantize_weight_blocks (struct fp8bq_weight)."""
+    _fields_ = [("w", ctypes.c_void_p), ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("ldw", ctypes.c_int64),
+                ("q", ctypes.c_void_p), ("qT", ctypes.c_void_p), ("s", ctypes.c_void_p)]
 
 
 def _load():
@@ -45,6 +51,7 @@ def _load():
         "fp8bq_quantize_rowcol": [vp, i32, i64, i64, i64, vp, vp, vp, vp, vp],
         "fp8bq_swiglu_quantize": [vp, i64, i64, i64, vp, vp, vp, vp, vp, vp],
         "fp8bq_quantize_weight_block": [vp, i32, i64, i64, i64, vp, vp, vp, vp],
+        "fp8bq_quantize_weight_blocks": [ctypes.POINTER(FP8BQWeight), i32, i32, vp],
         "fp8bq_gemm_fprop": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
         "fp8bq_gemm_fprop_q": [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, vp],
         "fp8bq_gemm_dgrad": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
@@ -195,6 +202,30 @@ def fp8bq_quantize_weight_block(w: torch.Tensor, q: torch.Tensor, qT: Optional[t
     with torch.cuda.device(w.device):
         _raise(lib.fp8bq_quantize_weight_block(_ptr(w), _dtype_code(w), N, K, ldw, _ptr(q), _ptr(qT), _ptr(s),
                                                _stream(w)), "fp8bq_quantize_weight_block")
+
+
+def fp8bq_quantize_weight_blocks(items) -> None:
+    """Several weights in one launch: items = [(w, q, qT or None, s), ...],
+    each as fp8bq_quantize_weight_block takes them, all of one dtype and on
+    one device."""
+    items = list(items)
+    if not items:
+        return
+    entries = (FP8BQWeight * len(items))()
+    dev, dt = items[0][0].device, items[0][0].dtype
+    for e, (w, q, qT, s) in zip(entries, items):
+        if w.device != dev or w.dtype != dt:
+            raise ValueError("fp8bq_quantize_weight_blocks: every weight must share device and dtype")
+        ldw = _rows_input(w, "w")
+        N, K = w.shape
+        _need(q, torch.uint8, (N, K), "q")
+        if qT is not None:
+            _need(qT, torch.uint8, (K, N), "qT")
+        _need(s, torch.float32, (N // 128, K // 128), "s")
+        e.w, e.N, e.K, e.ldw, e.q, e.qT, e.s = _ptr(w), N, K, ldw, _ptr(q), _ptr(qT), _ptr(s)
+    with torch.cuda.device(dev):
+        _raise(lib.fp8bq_quantize_weight_blocks(entries, len(items), _dtype_code(items[0][0]), _stream(items[0][0])),
+               "fp8bq_quantize_weight_blocks")
 
 
 def fp8bq_gemm_fprop(xq, sx, wq, sw, y) -> None:

@@ -132,9 +132,10 @@ fp8bq_status fp8bq_quantize_rowcol(const void* x, fp8bq_dtype dtype, int64_t M, 
  *   q      [M][F] row-wise codes,     s_row [F/128][M]
  *   qT     [F][M] column-wise codes,  s_col [M/128][F]
  * Requires M % 128 == 0, F % 128 == 0, ldgu >= 2F, 16-byte aligned pointers
- * and row pitch.  expf is the CUDA library's, so H may differ from a
- * correctly rounded silu(g) u by one BF16 ulp; the codes and scales are
- * always exactly those of the H the kernel formed.
+ * and row pitch.  H is formed in FP32 with a hardware exponential and a
+ * correctly rounded reciprocal (relative error far below half a BF16 ulp),
+ * so it may differ from a correctly rounded silu(g) u by one BF16 ulp; the
+ * codes and scales are always exactly those of the H the kernel formed.
  * Source: Puro-2B technical report (lkr-homepage blog), section 2 "FP8" for
  *   the quantization; the SwiGLU MLP of the 3.8B architecture in the n1n.ai
  *   "$998 3.8B" article, model-architecture list, for the gate.
@@ -155,6 +156,31 @@ fp8bq_status fp8bq_swiglu_quantize(const void* gu, int64_t M, int64_t F, int64_t
  */
 fp8bq_status fp8bq_quantize_weight_block(const void* w, fp8bq_dtype dtype, int64_t N, int64_t K, int64_t ldw,
                                          uint8_t* q, uint8_t* qT, float* s, fp8bq_stream_t stream);
+
+/* One weight of fp8bq_quantize_weight_blocks: the arguments of
+ * fp8bq_quantize_weight_block for that weight. */
+typedef struct {
+    const void* w;      /* [N][K] weight, row pitch ldw elements             */
+    int64_t N, K, ldw;
+    uint8_t* q;         /* [N][K] E4M3 codes                                 */
+    uint8_t* qT;        /* [K][N] the same codes transposed, or NULL to skip */
+    float* s;           /* [N/128][K/128] FP32 block scales                  */
+} fp8bq_weight;
+
+/*
+ * Weight quantization per 128x128 block for several weights in one launch
+ * (a training step quantizes every weight once after the optimizer update).
+ * Writes, for each entry, exactly what fp8bq_quantize_weight_block would,
+ * bit for bit.  All weights have element type `dtype`; the same requirements
+ * apply to each entry (entries with N or K == 0 are skipped); any entry that
+ * fails them fails the whole call before anything is launched.  count may be
+ * 0; lists longer than 16 are processed 16 entries per launch.  `weights`
+ * is a HOST array, read during the call only.
+ * Source: Puro-2B technical report (lkr-homepage blog), section 2 "FP8" (as
+ *   fp8bq_quantize_weight_block).
+ */
+fp8bq_status fp8bq_quantize_weight_blocks(const fp8bq_weight* weights, int count, fp8bq_dtype dtype,
+                                          fp8bq_stream_t stream);
 
 /*
  * Fprop: Y[m][n] = sum_c sx[c][m] * sw[n/128][c] * sum_{k in chunk c} D(xq[m][k]) D(wq[n][k])

@@ -166,3 +166,28 @@ def test_mx_entry_points_reject_bad_arguments_on_the_host(lib):
     assert m(P, P, P, P, None, 128, 128, 128, None) == ERR_NULL
     assert m(P, None, P, P, P, 128, 128, 128, None) == ERR_NULL
     assert m(P, P, P, P + 4, P, 128, 128, 128, None) == ERR_ALIGN
+
+
+def test_grouped_weight_quantizer_rejects_bad_arguments_on_the_host(lib):
+    from fp8_precision_pretraining_amax_b300.fp8bq import FP8BQWeight
+    f = lib.fp8bq_quantize_weight_blocks
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.POINTER(FP8BQWeight), ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+
+    def entries(*ws):
+        arr = (FP8BQWeight * len(ws))()
+        for e, (w, N, K, ldw, q, qT, s) in zip(arr, ws):
+            e.w, e.N, e.K, e.ldw, e.q, e.qT, e.s = w, N, K, ldw, q, qT, s
+        return arr
+    good = (P, 128, 256, 256, P, P, P)
+    assert f(None, 0, 0, None) == OK                       # nothing to do
+    assert f(None, 1, 0, None) == ERR_NULL
+    assert f(entries(good), -1, 0, None) == ERR_SHAPE
+    assert f(entries(good), 1, 7, None) == ERR_DTYPE
+    assert f(entries(good, (P, 100, 256, 256, P, P, P)), 2, 0, None) == ERR_SHAPE   # N % 128
+    assert f(entries(good, (P, 128, 256, 255, P, P, P)), 2, 0, None) == ERR_SHAPE   # pitch < width
+    assert f(entries(good, (0, 128, 256, 256, P, P, P)), 2, 0, None) == ERR_NULL    # no input
+    assert f(entries(good, (P, 128, 256, 256, P, None, None)), 2, 0, None) == ERR_NULL   # no scales
+    assert f(entries(good, (P + 8, 128, 256, 256, P, P, P)), 2, 0, None) == ERR_ALIGN
+    assert f(entries(good, (P, 128, 256, 260, P, P, P)), 2, 0, None) == ERR_ALIGN    # BF16 pitch 520 bytes
+    assert f(entries((P, 0, 256, 256, 0, 0, 0), (0, 128, 0, 0, 0, 0, 0)), 2, 0, None) == OK   # only empty weights

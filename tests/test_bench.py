@@ -95,7 +95,10 @@ def test_every_workload_plan_does_its_gemms_once(workload):
     want = {"layer_3p8b": 12, "swiglu": 2, "up_bwd": 2, "qkv_1p7b": 1, "tiny": 1}[workload]
     assert sum(k.startswith("gemm") for k in kinds) == want
     assert not any(k.startswith("comm") for k in kinds)
-    assert all(u.inputs and u.outputs for u in units)
+    assert all(u.inputs for u in units) and all(u.outputs for u in units if u.name != "weights")
+    if workload == "layer_3p8b":
+        assert units[0].name == "weights" and [k for k, _, _ in units[0].launches] == ["quant_weight"]
+        assert sum(k == "quant_weight" for k in kinds) == 1     # one launch for all four weights
     if workload == "swiglu":
         assert kinds == ["quant_weight", "quant_rowwise", "gemm_fprop", "quant_swiglu", "quant_weight", "gemm_fprop"]
     if workload == "up_bwd":
@@ -111,7 +114,7 @@ def test_data_parallel_plan_all_reduces_the_fp32_wgrad():
     shapes = bench.workload_shapes("layer_3p8b", tokens=256)
     lins = [_Lin(n, M, K, N) for n, M, K, N in shapes]
     units = bench.build_units(fp8bq, "layer_3p8b", lins, "cpu", 2)
-    for u in units:
+    for u in units[1:]:          # units[0] quantizes the weights
         kinds = [k for k, _, _ in u.launches]
         i = kinds.index("gemm_wgrad")
         assert kinds[i + 1] == "comm_allreduce_dw"

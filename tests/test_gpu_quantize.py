@@ -341,3 +341,54 @@ def test_swiglu_quantize_extremes_and_pitch(fb):
     big[1, :F] = -1e4
     gu = big.to(torch.bfloat16).cuda()
     _swiglu_case(fb, gu, F, "swiglu extremes")             # ldgu = 3F > 2F
+
+
+def _weight_items(ws, transpose_mask):
+    items = []
+    for w, t in zip(ws, transpose_mask):
+        N, K = w.shape
+        items.append((w, torch.empty((N, K), dtype=torch.uint8, device=w.device),
+                      torch.empty((K, N), dtype=torch.uint8, device=w.device) if t else None,
+                      torch.empty((N // 128, K // 128), dtype=torch.float32, device=w.device)))
+    return items
+
+
+def test_grouped_weight_quantizer_equals_one_call_per_weight(fb):
+    """The grouped launch writes, for every weight, exactly what the per-weight
+    quantizer writes (the 3.8B layer's four weights, one with the transposed
+    codes skipped, plus a special-value weight), and the oracle agrees."""
+    gen = synth.generator(310, "cuda")
+    ws = [synth.weight(N, K, gen, "cuda") for _, K, N in synth.LAYER_3P8B]
+    ws.append(_special_bf16(256, 384, 13).cuda())
+    mask = [True, False, True, True, True]
+    items = _weight_items(ws, mask)
+    fb.fp8bq_quantize_weight_blocks(items)
+    fb.check()
+    for (w, q, qT, s), t in zip(items, mask):
+        q1, qT1, s1 = fb.quantize_weight_block(w, transpose=t)
+        fb.check()
+        assert torch.equal(q, q1) and torch.equal(s, s1)
+        if t:
+            assert torch.equal(qT, qT1)
+    w, q, qT, s = items[-1]
+    qo, qTo, so = oracle.quantize_weight_block(host_input(w))
+    assert_codes_equal(q.cpu().numpy(), qo, "grouped specials codes")
+    assert_codes_equal(qT.cpu().numpy(), qTo, "grouped specials transposed codes")
+    assert_scales_equal(s.cpu().numpy(), so, "grouped specials scales")
+
+
+def test_grouped_weight_quantizer_long_list_fp32_and_empty(fb):
+    """More entries than one launch takes (processed in several launches),
+    FP32 weights, and an empty list."""
+    gen = synth.generator(311, "cuda")
+    ws = [synth.gaussian((128 * (1 + i % 3), 128 * (1 + i % 2)), 0.02, gen, "cuda") for i in range(19)]
+    items = _weight_items(ws, [i % 2 == 0 for i in range(19)])
+    fb.fp8bq_quantize_weight_blocks(items)
+    fb.fp8bq_quantize_weight_blocks([])
+    fb.check()
+    for i, (w, q, qT, s) in enumerate(items):
+        qo, qTo, so = oracle.quantize_weight_block(host_input(w))
+        assert_codes_equal(q.cpu().numpy(), qo, f"fp32 weight {i}")
+        assert_scales_equal(s.cpu().numpy(), so, f"fp32 weight {i} scales")
+        if qT is not None:
+            assert_codes_equal(qT.cpu().numpy(), qTo, f"fp32 weight {i} transposed")
