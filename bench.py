@@ -3,11 +3,13 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--tokens M]
                     [--impl reference] [--variant mx]
 
-One step is one pass of the whole hot path over one batch: for every linear
-of the workload, the weight-block quantizer (with the transposed copy), one
-pass over X producing its row-wise (Fprop) and column-wise (Wgrad) codes,
-Fprop, one pass over dY producing its row-wise (Dgrad) and column-wise
-(Wgrad) codes, Dgrad and Wgrad.
+One step is one pass of the whole hot path over one batch.  On the default
+workload: the weight-block quantizer over all of the layer's weights (codes
+and the transposed copy, one launch), then for every linear one pass over X
+producing its row-wise (Fprop) and column-wise (Wgrad) codes, Fprop, one pass
+over dY producing its row-wise (Dgrad) and column-wise (Wgrad) codes, Dgrad
+and Wgrad.  The other workloads run the launches of their configuration
+(--workload; see WORKLOAD_GEMMS).
 
 Metric: FP8 block-scaled GEMM TFLOP/s including quantization = sum of 2*M*N*K
 over the step's GEMMs divided by the step time (quantizers included), plus
@@ -32,9 +34,10 @@ GEMMs on the block-scaled MMA, which applies the scales itself.
 
 Multi-GPU (torchrun): data parallel with weak scaling.  Every rank runs the
 step on its own batch of the workload's size; Fprop and Dgrad need nothing
-from other ranks, and the dW of every linear is summed over the ranks with an
-NCCL all-reduce inside the timed step (the only exchange of the path).  The
-timed region is bracketed by barriers and the max over ranks is reported.
+from other ranks, each linear's Wgrad is computed in FP32
+(fp8bq_gemm_wgrad_f32) and that FP32 dW is summed over the ranks with an NCCL
+all-reduce inside the timed step (the only exchange of the path).  The timed
+region is bracketed by barriers and the max over ranks is reported.
 """
 from __future__ import annotations
 

@@ -147,6 +147,15 @@ __device__ __forceinline__ bool warp_wait_backoff(uint64_t* bar, uint32_t parity
     return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
 }
 
+// The reduction chunk a cluster's producers load i-th for the it-th tile the
+// cluster takes: odd tiles walk the reduction backwards.  The clusters take
+// their tiles in step, so a new tile starts on the chunks the previous wave
+// of tiles read last, which are still in L2, and the operands it shares with
+// that wave (the B column blocks of a row-major wave) come from L2 instead of
+// HBM.  Chunk partials are summed in that order; the result stays within
+// the same bound (any order of the FP32 sum over chunks is a valid reading).
+__device__ __forceinline__ int chunk_of(int i, int it, int KC) { return (it & 1) ? KC - 1 - i : i; }
+
 // Stop both CTAs of the pair and record the timeout.
 __device__ __forceinline__ void raise_abort(GemmCtl* ctl, uint32_t peer_abort, unsigned int* status) {
     if ((threadIdx.x & 31) == 0) {
@@ -247,11 +256,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t full0 = mapa_shared(smem_addr(&ctl->full[0]), 0);
         uint32_t s = 0, ph = 0, issued = 0;
         bool ok = true;
-        for (int tile = first_tile; tile < p.num_tiles && ok; tile += tile_step) {
+        int it = 0;
+        for (int tile = first_tile; tile < p.num_tiles && ok; tile += tile_step, ++it) {
             const int tm = tile / p.tiles_n, tn = tile - tm * p.tiles_n;
             const int r0 = tm * kPairM + static_cast<int>(rank) * kBM;  // this CTA's first row
             const int b0 = tn * kBN + static_cast<int>(rank) * kBNHalf;  // this CTA's first B row
-            for (int c = 0; c < p.KC; ++c) {
+            for (int i = 0; i < p.KC; ++i) {
+                const int c = chunk_of(i, it, p.KC);
                 if (!warp_wait(&ctl->empty[s], ph ^ 1, abort_flag, lim)) { ok = false; break; }
                 if (lane == 0) {
                     if (leader) mbar_arrive_expect_tx(&ctl->full[s], 2 * (kStageBytesA + kStageBytesB));
@@ -274,13 +285,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // the problem are skipped.
         uint32_t q = 0, qph = 0, issued = 0;
         bool ok = true;
-        for (int tile = first_tile; tile < p.num_tiles && ok; tile += tile_step) {
+        int it = 0;
+        for (int tile = first_tile; tile < p.num_tiles && ok; tile += tile_step, ++it) {
             const int tm = tile / p.tiles_n, tn = tile - tm * p.tiles_n;
             const int r0 = tm * kPairM + static_cast<int>(rank) * kBM;
             const int j0 = tn * kBN;
             const uint32_t a_bytes = r0 < p.I ? 128u * 4u : 0u;
             const uint32_t b_bytes = MODE == kModeWgrad ? static_cast<uint32_t>(min(p.J - j0, kBN)) * 4u : 0u;
-            for (int c = 0; c < p.KC; ++c) {
+            for (int i = 0; i < p.KC; ++i) {
+                const int c = chunk_of(i, it, p.KC);
                 if (!warp_wait_backoff(&ctl->sempty[q], qph ^ 1, abort_flag, lim)) { ok = false; break; }
                 ScaleSlot& sl = ctl->scl[q];
                 if (lane == 0) {
@@ -368,9 +381,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (int c = 0; c < p.KC; ++c) {
                 if (!warp_wait(&ctl->sfull[q], qph, abort_flag, lim)) { ok = false; break; }
                 const ScaleSlot& sl = ctl->scl[q];
-                const float sa = sl.a[row];
-                const float sab = MODE == kModeWgrad ? 0.0f : sa * sl.b[half];
-                const float* sbs = &sl.b[half * 128];   // Wgrad column scales of this half
+                const float sab = MODE == kModeWgrad ? 0.0f : sl.a[row] * sl.b[half];
+                // Wgrad: this thread's row scales (see load_group) and the
+                // column scales of this half, by shared-window address
+                const uint32_t sas = smem_addr(&sl.a[quarter * 32 + (lane >> 2)]);
+                const uint32_t sbs = smem_addr(&sl.b[half * 128 + 2 * (lane & 3)]);
                 if (!warp_wait(&ctl->tfull[buf], tph, abort_flag, lim)) { ok = false; break; }
                 // the MMA that produced this partial has read the chunk's
                 // operand stage: this CTA's producer may refill it
@@ -378,45 +393,72 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 if (++stage == kStages) stage = 0;
                 tc_fence_after();
                 const uint32_t tbase = tmem + lane_off + buf * kBN + half * 128;
+                // The partial in four groups of 32 values per thread.
+                // Fprop/Dgrad (32x32b shape): the thread's row (its TMEM lane),
+                // columns 32g .. 32g + 31.  Wgrad (16x256b shape): lanes
+                // 16(g & 1) + lane/4 and + 8 of this warp's quarter, columns
+                // 64(g >> 1) + 8k + 2(lane % 4) + {0, 1} for k < 8, so that a
+                // thread needs 32 of the chunk's column scales instead of 128
+                // (the scales reach every lane through shared-memory
+                // broadcasts, one 128-byte wavefront per 128 bytes that the
+                // warp receives).
+                auto load_group = [&](int g, uint32_t (&v)[32]) {
+                    if (MODE != kModeWgrad)
+                        tmem_ld_32x32b_x32(tbase + 32 * g, v);
+                    else
+                        tmem_ld_16x256b_x8(tbase + (static_cast<uint32_t>((g & 1) * 16) << 16) + (g >> 1) * 64, v);
+                };
+                // Wgrad: the column scales of groups 2h and 2h + 1 (the same
+                // columns of the two 16-lane halves), loaded once for both
+                float2 sbv[8];
+                auto load_col_scales = [&](int h) {
+                    if (MODE == kModeWgrad) {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) sbv[k] = lds_f32x2(sbs + h * 256 + 32 * k);
+                    }
+                };
                 // acc += (sA * sB) * partial (Fprop, Dgrad), or
-                // acc += sA * (sB[j] * partial) (Wgrad), 32 columns at a time.
+                // acc += sA * (sB[j] * partial) (Wgrad).
                 auto promote = [&](const uint32_t (&v)[32], int g) {
                     float* a = acc + g * 32;
                     if (MODE != kModeWgrad) {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) a[i] = __fmaf_rn(sab, __uint_as_float(v[i]), a[i]);
                     } else {
+                        const float s0 = lds_f32(sas + (g & 1) * 64), s1 = lds_f32(sas + (g & 1) * 64 + 32);
 #pragma unroll
-                        for (int i = 0; i < 32; i += 4) {
-                            const float4 b = *reinterpret_cast<const float4*>(sbs + g * 32 + i);
+                        for (int k = 0; k < 8; ++k) {
+                            const float2 b = sbv[k];
                             float t0, t1, t2, t3;
-                            fmul2(t0, t1, __uint_as_float(v[i]), __uint_as_float(v[i + 1]), b.x, b.y);
-                            fmul2(t2, t3, __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]), b.z, b.w);
-                            ffma2(a[i], a[i + 1], t0, t1, sa, sa);
-                            ffma2(a[i + 2], a[i + 3], t2, t3, sa, sa);
+                            fmul2(t0, t1, __uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]), b.x, b.y);
+                            fmul2(t2, t3, __uint_as_float(v[4 * k + 2]), __uint_as_float(v[4 * k + 3]), b.x, b.y);
+                            ffma2(a[4 * k], a[4 * k + 1], t0, t1, s0, s0);
+                            ffma2(a[4 * k + 2], a[4 * k + 3], t2, t3, s1, s1);
                         }
                     }
                 };
-                // Two 32-column staging buffers: groups 0 and 1 load together,
+                // Two 32-value staging buffers: groups 0 and 1 load together,
                 // group 2 loads while group 0 is multiplied in, group 3 while
                 // group 1 is; the TMEM buffer goes back to the MMA as soon as
                 // group 3 is in registers.
                 uint32_t ra[32], rb[32];
-                tmem_ld_32x32b_x32(tbase, ra);
-                tmem_ld_32x32b_x32(tbase + 32, rb);
+                load_group(0, ra);
+                load_group(1, rb);
                 tmem_wait_ld();
                 reg_fence32(ra);
                 reg_fence32(rb);
+                load_col_scales(0);
                 promote(ra, 0);
-                tmem_ld_32x32b_x32(tbase + 64, ra);
+                load_group(2, ra);
                 promote(rb, 1);
-                tmem_ld_32x32b_x32(tbase + 96, rb);
+                load_group(3, rb);
                 tmem_wait_ld();
                 reg_fence32(ra);
                 reg_fence32(rb);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(tempty0 + buf * 8);
+                load_col_scales(1);
                 promote(ra, 2);
                 promote(rb, 3);
                 __syncwarp();
@@ -440,12 +482,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     for (int bx = 0; bx < 4; ++bx) {
                         if (lane == 0) bulk_wait_group_read<0>();
                         __syncwarp();
+                        if (MODE != kModeWgrad) {
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const float* a = acc + bx * 32 + j * 8;
-                            *reinterpret_cast<uint4*>(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
-                                make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]),
-                                           pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7]));
+                            for (int j = 0; j < 4; ++j) {
+                                const float* a = acc + bx * 32 + j * 8;
+                                *reinterpret_cast<uint4*>(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
+                                    make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]),
+                                               pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7]));
+                            }
+                        } else {
+                            // Wgrad layout: box bx holds repetitions 4(bx & 1) ..
+                            // + 3 of groups 2(bx >> 1) and + 1, two rows each
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                const int lh = e >> 3, kk = (e >> 1) & 3, rs = e & 1;
+                                const float* a = acc + (lh + 2 * (bx >> 1)) * 32 + 4 * (4 * (bx & 1) + kk) + 2 * rs;
+                                const int R = lh * 16 + rs * 8 + (lane >> 2);
+                                *reinterpret_cast<uint32_t*>(stg + R * 64 + ((kk ^ ((R >> 1) & 3)) << 4) + 4 * (lane & 3)) =
+                                    pack_bf16x2(a[0], a[1]);
+                            }
                         }
                         fence_proxy_async_smem();
                         __syncwarp();
@@ -521,11 +576,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 for (int bx = 0; bx < 8; ++bx) {
                     if (lane == 0) bulk_wait_group_read<0>();
                     __syncwarp();
+                    if (MODE != kModeWgrad) {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const float* a = acc + bx * 16 + j * 4;
-                        *reinterpret_cast<float4*>(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
-                            make_float4(a[0], a[1], a[2], a[3]);
+                        for (int j = 0; j < 4; ++j) {
+                            const float* a = acc + bx * 16 + j * 4;
+                            *reinterpret_cast<float4*>(stg + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
+                                make_float4(a[0], a[1], a[2], a[3]);
+                        }
+                    } else {
+                        // Wgrad layout: box bx holds repetitions 2(bx & 3) and
+                        // + 1 of groups 2(bx >> 2) and + 1, two rows each
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int lh = e >> 2, kk = (e >> 1) & 1, rs = e & 1;
+                            const float* a = acc + (lh + 2 * (bx >> 2)) * 32 + 4 * (2 * (bx & 3) + kk) + 2 * rs;
+                            const int R = lh * 16 + rs * 8 + (lane >> 2);
+                            const int C = 8 * kk + 2 * (lane & 3);   // column within the box
+                            *reinterpret_cast<float2*>(stg + R * 64 + (((C >> 2) ^ ((R >> 1) & 3)) << 4) + (C & 3) * 4) =
+                                make_float2(a[0], a[1]);
+                        }
                     }
                     fence_proxy_async_smem();
                     __syncwarp();

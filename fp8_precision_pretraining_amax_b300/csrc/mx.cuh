@@ -404,9 +404,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         // ----------------------------------------------------- operand producer
         uint32_t s = 0, ph = 0, issued = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+        int it = 0;
+        for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x, ++it) {
             const int tm = tile / p.tiles_n, tn = tile - tm * p.tiles_n;
-            for (int c = 0; c < p.KC; ++c) {
+            for (int i = 0; i < p.KC; ++i) {
+                const int c = chunk_of(i, it, p.KC);  // odd tiles walk the reduction backwards
                 if (!warp_wait(&ctl->empty[s], ph ^ 1, abort_flag, lim)) { ok = false; break; }
                 if (lane == 0) {
                     const uint32_t fb = smem_addr(&ctl->full[s]);
@@ -424,11 +426,13 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         // -------------------------------------------------- exponent producer
         uint32_t q = 0, qph = 0, issued = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
+        int it = 0;
+        for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x, ++it) {
             const int tm = tile / p.tiles_n, tn = tile - tm * p.tiles_n;
             const int j0 = tn * kMxBN;
             const uint32_t b_bytes = static_cast<uint32_t>(min(p.J - j0, kMxBN)) * 4u;
-            for (int c = 0; c < p.KC; ++c) {
+            for (int i = 0; i < p.KC; ++i) {
+                const int c = chunk_of(i, it, p.KC);  // the operand producer's order
                 if (!warp_wait_backoff(&ctl->sempty[q], qph ^ 1, abort_flag, lim)) { ok = false; break; }
                 if (lane == 0) {
                     MxSfSlot& sl = ctl->sf[q];

@@ -42,8 +42,11 @@
  *     untouched.  A failed launch returns FP8BQ_ERR_CUDA.  Device-side faults
  *     the kernels detect themselves (a pipeline wait that ran out of time)
  *     are recorded in a per-device status word and reported by fp8bq_check.
- *   - The library is thread-safe; it keeps only a per-device status word and
- *     a cache of device properties, both created on first use.
+ *   - The library is thread-safe; it keeps only a per-device status word, a
+ *     cache of device properties and a mutex-guarded cache of the TMA
+ *     descriptors it encoded (keyed by every argument of the encoding, so a
+ *     buffer reused with the same shape is not encoded again), all created on
+ *     first use.
  */
 #ifndef FP8BQ_H
 #define FP8BQ_H
