@@ -28,12 +28,8 @@
 //               thread issues four tcgen05.mma.cta_group::2.kind::f8f6f4
 //               (256x256x32) per chunk into one of two TMEM partial buffers
 //               of 256 FP32 columns, started fresh every chunk, then commits
-//               with a multicast to both CTAs' partial-full barriers.  The
-//               completed partial also means the stage was read: in Fprop and
-//               Dgrad the first promotion warp of each CTA then frees the
-//               stage for its producer, keeping one commit off the MMA
-//               thread's critical path; in Wgrad (promotion-bound) the MMA
-//               commits to the stage-empty barriers as well.
+//               with a multicast to both CTAs' stage-empty barriers (the
+//               producers may refill the stage) and partial-full barriers.
 //   warp 3      idle (the first warpgroup gives up registers: 40 per thread)
 //   warps 4..11 promotion (two warpgroups at 232 registers per thread, both
 //               CTAs): each thread owns one output row and 128 columns; it
@@ -110,7 +106,7 @@ struct alignas(16) ScaleSlot {
 
 struct alignas(16) GemmCtl {
     uint64_t full[kStages];    // even CTA: both CTAs' bytes of the stage landed
-    uint64_t empty[kStages];   // both CTAs: the pair MMA has read the stage (signalled by promotion warp 0)
+    uint64_t empty[kStages];   // both CTAs: the pair MMA has read the stage
     uint64_t tfull[2];         // both CTAs: the chunk partial is in TMEM
     uint64_t tempty[2];        // even CTA: both CTAs' promotion warps read it
     uint64_t sfull[kScaleSlots];   // the slot's scale copies landed
@@ -245,7 +241,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     volatile int* abort_flag = &ctl->abort;
     const uint32_t peer_abort = mapa_shared(smem_addr(&ctl->abort), rank ^ 1u);
     const uint64_t lim = p.timeout_ns;
-    constexpr bool kStageFreedByMma = MODE == kModeWgrad;
 
     // Register split (launch: 384 x 168): warpgroup 0 keeps 40, the two
     // promotion warpgroups take 232 each; 128*40 + 256*232 == 384*168.
@@ -341,11 +336,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     for (int k = 0; k < kBK / 32; ++k)
                         mma_e4m3_pair(d, sw128_kmajor_desc(a0 + 32 * k), sw128_kmajor_desc(b0 + 32 * k), idesc,
                                       k > 0);
-                    // Fprop/Dgrad: one commit per chunk (the completed partial
-                    // also means the stage was read; a promotion warp hands the
-                    // stage back).  Wgrad, whose promotion is the slower side,
-                    // frees the stage from the MMA itself.
-                    if (kStageFreedByMma) mma_commit_pair_mc(smem_addr(&ctl->empty[s]), 0x3);
+                    // the stage is free once these MMAs have read it; the
+                    // partial is ready once they have completed
+                    mma_commit_pair_mc(smem_addr(&ctl->empty[s]), 0x3);
                     mma_commit_pair_mc(smem_addr(&ctl->tfull[buf]), 0x3);
                     if (++s == kStages) { s = 0; ph ^= 1; }
                     buf ^= 1;
@@ -366,7 +359,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int row = quarter * 32 + lane;   // tile row == TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t tempty0 = mapa_shared(smem_addr(&ctl->tempty[0]), 0);
-        uint32_t buf = 0, tph = 0, q = 0, qph = 0, stage = 0;
+        uint32_t buf = 0, tph = 0, q = 0, qph = 0;
         bool ok = true;
         for (int tile = first_tile; tile < p.num_tiles && ok; tile += tile_step) {
             const int tm = tile / p.tiles_n, tn = tile - tm * p.tiles_n;
@@ -387,10 +380,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const uint32_t sas = smem_addr(&sl.a[quarter * 32 + (lane >> 2)]);
                 const uint32_t sbs = smem_addr(&sl.b[half * 128 + 2 * (lane & 3)]);
                 if (!warp_wait(&ctl->tfull[buf], tph, abort_flag, lim)) { ok = false; break; }
-                // the MMA that produced this partial has read the chunk's
-                // operand stage: this CTA's producer may refill it
-                if (!kStageFreedByMma && pw == 0 && lane == 0) mbar_arrive(&ctl->empty[stage]);
-                if (++stage == kStages) stage = 0;
                 tc_fence_after();
                 const uint32_t tbase = tmem + lane_off + buf * kBN + half * 128;
                 // The partial in four groups of 32 values per thread.
