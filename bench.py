@@ -303,11 +303,24 @@ def step_launches_mx(fp8bq, L, lin):
 class Unit:
     """One part of the step: its launches, the input tensors a user would
     bring from the host and the outputs a user would take back (the
-    end-to-end leg moves exactly these)."""
+    end-to-end leg moves exactly these).  reads[j] = (first, last): the
+    launches that first and last read input j; ready[j]: the launch after
+    which output j is complete (defaults: every launch reads every input,
+    outputs are complete after the last launch)."""
 
-    def __init__(self, name, launches, inputs, outputs, setup=()):
+    def __init__(self, name, launches, inputs, outputs, setup=(), reads=None, ready=None):
         self.name, self.launches, self.inputs, self.outputs = name, launches, list(inputs), list(outputs)
         self.setup = list(setup)   # calls made once before the first step (not timed)
+        n = len(launches)
+        self.reads = list(reads) if reads is not None else [(0, n - 1)] * len(self.inputs)
+        self.ready = list(ready) if ready is not None else [n - 1] * len(self.outputs)
+        assert len(self.reads) == len(self.inputs) and len(self.ready) == len(self.outputs)
+        assert all(0 <= f <= l < n for f, l in self.reads) and all(0 <= r < n for r in self.ready)
+
+
+def launch_index(launches, kind, nth=0):
+    """Index of the nth launch of `kind` in a launch list."""
+    return [i for i, (k, _, _) in enumerate(launches) if k == kind][nth]
 
 
 def data_parallel_wgrad(fp8bq, L, launches, dist):
@@ -340,7 +353,7 @@ def build_units(fp8bq, name, lins, dev, world, variant="fp32-scale"):
             wl = [(lin.w, L.wq, L.wqT, L.sw) for L, lin in zip(layers, lins)]
             units.append(Unit("weights", [("quant_weight", sum(weight_bytes(l.N, l.K) for l in lins),
                                            lambda: fp8bq.fp8bq_quantize_weight_blocks(wl))],
-                              [lin.w for lin in lins], []))
+                              [lin.w for lin in lins], [], reads=[(0, 0)] * len(lins)))
         for L, lin in zip(layers, lins):
             launches = step_launches_mx(fp8bq, L, lin) if mx else step_launches(fp8bq, L, lin)[1:]
             dw = L.dw
@@ -349,7 +362,17 @@ def build_units(fp8bq, name, lins, dev, world, variant="fp32-scale"):
                                  lambda L=L: dist.all_reduce(L.dw, op=dist.ReduceOp.SUM)))
             elif world > 1:
                 dw = data_parallel_wgrad(fp8bq, L, launches, dist)
-            units.append(Unit(lin.name, launches, (lin.x, lin.w, lin.dy) if mx else (lin.x, lin.dy), (L.y, L.dx, dw)))
+            last = len(launches) - 1
+            if mx:
+                q = "quant_mx_rowcol"
+                reads = [(launch_index(launches, q, 1),) * 2, (launch_index(launches, q, 0),) * 2,
+                         (launch_index(launches, q, 2),) * 2]
+                ready = [launch_index(launches, "gemm_mx_fprop"), launch_index(launches, "gemm_mx_dgrad"), last]
+            else:
+                reads = [(launch_index(launches, "quant_rowcol", 0),) * 2, (launch_index(launches, "quant_rowcol", 1),) * 2]
+                ready = [launch_index(launches, "gemm_fprop"), launch_index(launches, "gemm_dgrad"), last]
+            units.append(Unit(lin.name, launches, (lin.x, lin.w, lin.dy) if mx else (lin.x, lin.dy), (L.y, L.dx, dw),
+                              reads=reads, ready=ready))
     elif name == "swiglu":
         gu_lin, down_lin = lins
         M, D, F = gu_lin.M, gu_lin.K, down_lin.K
@@ -366,7 +389,8 @@ def build_units(fp8bq, name, lins, dev, world, variant="fp32-scale"):
              lambda: fp8bq.fp8bq_quantize_weight_block(down_lin.w, mlp.wdq, None, mlp.swd)),
             ("gemm_fprop", 2 * M * D * F, lambda: fp8bq.fp8bq_gemm_fprop(mlp.hq, mlp.sh, mlp.wdq, mlp.swd, mlp.out)),
         ]
-        units.append(Unit("mlp", launches, (gu_lin.x, gu_lin.w, down_lin.w), (mlp.out,)))
+        units.append(Unit("mlp", launches, (gu_lin.x, gu_lin.w, down_lin.w), (mlp.out,),
+                          reads=[(1, 1), (0, 0), (4, 4)]))
     elif name == "up_bwd":
         lin = lins[0]
         M, K, N = lin.M, lin.K, lin.N
@@ -381,7 +405,8 @@ def build_units(fp8bq, name, lins, dev, world, variant="fp32-scale"):
         dw = data_parallel_wgrad(fp8bq, L, launches, dist) if world > 1 else L.dw
         # the weight's codes (and transposed codes) come from the forward pass
         setup = [lambda: fp8bq.fp8bq_quantize_weight_block(lin.w, L.wq, L.wqT, L.sw)]
-        units.append(Unit(lin.name, launches, (lin.x, lin.dy), (L.dx, dw), setup=setup))
+        units.append(Unit(lin.name, launches, (lin.x, lin.dy), (L.dx, dw), setup=setup,
+                          reads=[(0, 0), (1, 1)], ready=[launch_index(launches, "gemm_dgrad"), len(launches) - 1]))
     else:  # Fprop only: qkv_1p7b, tiny
         lin = lins[0]
         M, K, N = lin.M, lin.K, lin.N
@@ -393,7 +418,7 @@ def build_units(fp8bq, name, lins, dev, world, variant="fp32-scale"):
             ("quant_rowwise", rowwise_bytes(M, K, in_bytes=eb), lambda: fp8bq.fp8bq_quantize_rowwise(lin.x, L.xq, L.sx)),
             ("gemm_fprop", 2 * M * N * K, lambda: fp8bq.fp8bq_gemm_fprop(L.xq, L.sx, L.wq, L.sw, L.y)),
         ]
-        units.append(Unit(lin.name, launches, (lin.x, lin.w), (L.y,)))
+        units.append(Unit(lin.name, launches, (lin.x, lin.w), (L.y,), reads=[(1, 1), (0, 0)]))
     return units
 
 
@@ -554,36 +579,49 @@ def run_e2e(args, units, dev, flops, world, barrier):
     h2d = sum(t.numel() * t.element_size() for hs in host_in for t in hs)
     d2h = sum(t.numel() * t.element_size() for hs in host_out for t in hs)
 
-    # Three streams: host->device copies of unit i+1 and device->host copies
-    # of unit i-1 run while unit i computes (PCIe is full duplex).  Events
-    # keep each buffer's reuse in order across units and steps.
+    # Three streams.  Host->device copies run ahead on their own stream, each
+    # into a buffer as soon as the previous step's last reader of it has run;
+    # the compute stream waits for an input just before its first reader;
+    # each output goes device->host on the third stream as soon as the
+    # launch that completes it has run, while the rest of the step computes
+    # (PCIe is full duplex).  Events keep each buffer's reuse in order
+    # across units and steps.
     comp = torch.cuda.current_stream(dev)
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    n = len(units)
-    ev_in = [torch.cuda.Event() for _ in range(n)]
-    ev_comp = [torch.cuda.Event() for _ in range(n)]
-    ev_out = [torch.cuda.Event() for _ in range(n)]
-    for i in range(n):  # everything starts free
-        ev_comp[i].record(comp)
-        ev_out[i].record(s_out)
+    ev_free = [[torch.cuda.Event() for _ in u.inputs] for u in units]    # last reader of the input ran
+    ev_in = [[torch.cuda.Event() for _ in u.inputs] for u in units]      # the input is on the device
+    ev_ready = [[torch.cuda.Event() for _ in u.outputs] for u in units]  # the output is complete
+    ev_out = [[torch.cuda.Event() for _ in u.outputs] for u in units]    # the output is on the host
+    for i in range(len(units)):  # everything starts free
+        for e in ev_free[i]:
+            e.record(comp)
+        for e in ev_out[i]:
+            e.record(s_out)
 
     def e2e_step():
         for i, (u, hin, hout) in enumerate(zip(units, host_in, host_out)):
             with torch.cuda.stream(s_in):
-                s_in.wait_event(ev_comp[i])          # last step's compute has read these inputs
-                for d, h in zip(u.inputs, hin):
+                for j, (d, h) in enumerate(zip(u.inputs, hin)):
+                    s_in.wait_event(ev_free[i][j])
                     d.copy_(h, non_blocking=True)
-                ev_in[i].record(s_in)
-            comp.wait_event(ev_in[i])
-            comp.wait_event(ev_out[i])               # last step's outputs have left the device
-            for _, _, fn in u.launches:
+                    ev_in[i][j].record(s_in)
+            for e in ev_out[i]:                      # last step's outputs have left the device
+                comp.wait_event(e)
+            for k, (_, _, fn) in enumerate(u.launches):
+                for j, (first, _) in enumerate(u.reads):
+                    if first == k:
+                        comp.wait_event(ev_in[i][j])
                 fn()
-            ev_comp[i].record(comp)
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(ev_comp[i])
-                for h, d in zip(hout, u.outputs):
-                    h.copy_(d, non_blocking=True)
-                ev_out[i].record(s_out)
+                for j, (_, last) in enumerate(u.reads):
+                    if last == k:
+                        ev_free[i][j].record(comp)
+                for j, r in enumerate(u.ready):
+                    if r == k:
+                        ev_ready[i][j].record(comp)
+                        with torch.cuda.stream(s_out):
+                            s_out.wait_event(ev_ready[i][j])
+                            hout[j].copy_(u.outputs[j], non_blocking=True)
+                            ev_out[i][j].record(s_out)
 
     for _ in range(2):
         e2e_step()
@@ -604,9 +642,9 @@ def run_e2e(args, units, dev, flops, world, barrier):
         dt = float(t.item())
     return {"value": flops * world * steps / dt / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": 1e3 * dt / steps,
-            "path": ("pinned host -> device copies of each unit's inputs, the unit's C-ABI launches, device -> "
-                     "pinned host copies of its outputs; copies of neighbouring units overlap compute on "
-                     "separate streams")}
+            "path": ("pinned host -> device copies of every input, the C-ABI launches, device -> pinned host "
+                     "copies of every output; each input is copied as soon as its buffer is free and each output "
+                     "as soon as it is complete, on two copy streams that overlap compute")}
 
 
 # ---------------------------------------------------------------------------
