@@ -17,7 +17,7 @@
 // [128 r, 128 r + 128) of the tile and all 256 columns.
 //   warp 0      operand producer (both CTAs): TMA loads of this CTA's 128
 //               rows of A and its half (128 rows) of B per chunk into a
-//               6-stage shared-memory ring (128-byte swizzle), completion
+//               5-stage shared-memory ring (128-byte swizzle), completion
 //               bytes counted on the even CTA's full barrier, which expects
 //               both CTAs' bytes.
 //   warp 2      scale producer (both CTAs): bulk and cp.async copies of each
@@ -68,7 +68,7 @@ constexpr int kBN = 256;          // tile columns (MMA N)
 constexpr int kBNHalf = 128;      // B rows each CTA loads
 constexpr int kBRows = kBNHalf;   // B box height of the tensor map (rows per CTA)
 constexpr int kBK = 128;          // one scale chunk of the reduction
-constexpr int kStages = 6;
+constexpr int kStages = 5;
 constexpr int kScaleSlots = 6;
 constexpr int kGemmThreads = 384;
 constexpr int kFirstPromoWarp = 4;
@@ -77,10 +77,13 @@ constexpr uint32_t kStageBytesA = kBM * kBK;
 constexpr uint32_t kStageBytesB = kBNHalf * kBK;
 constexpr uint32_t kTmemCols = 2 * kBN;
 // Epilogue staging: a promotion warp writes its 32 rows x 128 BF16 columns
-// as four 32 x 32 boxes (64-byte rows, 64-byte swizzle) through one 2 KB
-// staging buffer (shared memory goes to the operand ring instead).
+// as four 32 x 32 boxes (64-byte rows, 64-byte swizzle) through three 2 KB
+// staging boxes used in rotation, so a box is written while the TMA stores
+// of the two before it are still reading theirs.  (A sixth operand stage
+// measured slower than the second and third staging box on GEMMs with a
+// short reduction, and no faster on long ones.)
 constexpr uint32_t kEpiBoxBytes = 32 * 64;
-constexpr uint32_t kEpiWarpBytes = kEpiBoxBytes;
+constexpr uint32_t kEpiWarpBytes = 3 * kEpiBoxBytes;   // three staging boxes per warp
 
 struct GemmParams {
     const float* sA;
@@ -360,6 +363,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t tempty0 = mapa_shared(smem_addr(&ctl->tempty[0]), 0);
         uint32_t buf = 0, tph = 0, q = 0, qph = 0;
+        int nbox = 0;   // staging box of the next BF16 output box
         bool ok = true;
         for (int tile = first_tile; tile < p.num_tiles && ok; tile += tile_step) {
             const int tm = tile / p.tiles_n, tn = tile - tm * p.tiles_n;
@@ -469,7 +473,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     // BF16 only: round while staging, four boxes of 32 x 32
 #pragma unroll
                     for (int bx = 0; bx < 4; ++bx) {
-                        if (lane == 0) bulk_wait_group_read<0>();
+                        // three staging boxes in rotation: the store that last
+                        // read this one is at least the third most recent
+                        uint8_t* stg = smEpi + pw * kEpiWarpBytes + nbox * kEpiBoxBytes;
+                        if (++nbox == 3) nbox = 0;
+                        if (lane == 0) bulk_wait_group_read<2>();
                         __syncwarp();
                         if (MODE != kModeWgrad) {
 #pragma unroll
