@@ -297,6 +297,16 @@ __device__ __forceinline__ float swiglu_f32(float g, float u) {
     return __fmul_rn(__fmul_rn(g, __frcp_rn(__fadd_rn(1.0f, __expf(-g)))), u);
 }
 
+// swiglu_f32 with the hardware reciprocal approximation (relative error about
+// 2^-23) in place of the correctly rounded one: the same bound holds, but the
+// approximation flushes results below 2^-126 to zero, so it is only used
+// when g > -87 (1 + exp(-g) < 2^126).
+__device__ __forceinline__ float swiglu_f32_fast(float g, float u) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(__fadd_rn(1.0f, __expf(-g))));
+    return __fmul_rn(__fmul_rn(g, r), u);
+}
+
 // Shared-memory scratch of one slab's processing (besides the slab itself).
 template <bool kF32>
 struct SlabScratch {
@@ -359,11 +369,23 @@ __device__ __forceinline__ void slab_process(uint8_t* __restrict__ slab, SlabScr
             const uint4 uw = *reinterpret_cast<const uint4*>(slab + 128 * RB + row * RB + ch * 16);
             const uint32_t gv[4] = {gw.x, gw.y, gw.z, gw.w}, uv[4] = {uw.x, uw.y, uw.z, uw.w};
             uint32_t hv[4];
+            bool fast = true;
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                __nv_bfloat162 hb = __floats2bfloat162_rn(swiglu_f32(bf16lo(gv[m]), bf16lo(uv[m])),
-                                                          swiglu_f32(bf16hi(gv[m]), bf16hi(uv[m])));
-                hv[m] = *reinterpret_cast<uint32_t*>(&hb);
+            for (int m = 0; m < 4; ++m) fast = fast && bf16lo(gv[m]) > -87.0f && bf16hi(gv[m]) > -87.0f;
+            if (__all_sync(0xFFFFFFFFu, fast)) {   // the whole warp takes the fast form
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    __nv_bfloat162 hb = __floats2bfloat162_rn(swiglu_f32_fast(bf16lo(gv[m]), bf16lo(uv[m])),
+                                                              swiglu_f32_fast(bf16hi(gv[m]), bf16hi(uv[m])));
+                    hv[m] = *reinterpret_cast<uint32_t*>(&hb);
+                }
+            } else {
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    __nv_bfloat162 hb = __floats2bfloat162_rn(swiglu_f32(bf16lo(gv[m]), bf16lo(uv[m])),
+                                                              swiglu_f32(bf16hi(gv[m]), bf16hi(uv[m])));
+                    hv[m] = *reinterpret_cast<uint32_t*>(&hb);
+                }
             }
             const uint4 hw = make_uint4(hv[0], hv[1], hv[2], hv[3]);
             *gp = hw;
