@@ -21,6 +21,9 @@ Default workload (layer_3p8b): one 3.8B-shaped transformer layer at 32768
 tokens (hidden 3072, 32 q / 8 kv heads of 96, SwiGLU FFN 8192): QKV
 3072->4608, O 3072->3072, gate+up 3072->16384, down 8192->3072.
 
+On one GPU the step's launches are captured once into a CUDA graph and the
+timed steps replay it (--no-graph times eager launches instead).
+
 Also reported: per-launch CUDA-event times (the roofline of the GEMM kernel
 against the FP8 tensor peak, the quantizers against HBM), the same metric
 end to end through the Python API with pinned host buffers (host->device
@@ -80,6 +83,8 @@ def parse_args(argv=None):
     ap.add_argument("--variant", default="fp32-scale", choices=["fp32-scale", "mx"],
                     help="fp32-scale: the layer's FP32 amax/448 scales per 1x128 tile / 128x128 block with "
                          "per-chunk promotion; mx: power-of-two scale per 1x32 block applied inside the MMA")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time eager launches instead of a CUDA graph of the step (one GPU)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args(argv)
@@ -457,8 +462,23 @@ def run_ours(args, rank, world, local_rank):
                     e1.record()
                     record.append((kind, work, e0, e1))
 
+    # One GPU: the step's launches are captured once into a CUDA graph and
+    # the timed steps replay it (no host launch overhead between kernels).
+    # Several GPUs: eager launches (the NCCL all-reduce stays outside graphs).
+    run_step = step
+    if world == 1 and not args.no_graph:
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            step()                      # first calls (descriptor encoding, attributes) outside capture
+        torch.cuda.current_stream(dev).wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        run_step = graph.replay
     for _ in range(args.warmup):
-        step()
+        run_step()
     fp8bq.check(dev)
     torch.cuda.synchronize()
 
@@ -470,7 +490,7 @@ def run_ours(args, rank, world, local_rank):
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record()
         for _ in range(args.steps):
-            step()
+            run_step()
         t1.record()
         torch.cuda.synchronize()
     barrier()
@@ -537,6 +557,8 @@ def run_ours(args, rank, world, local_rank):
     else:
         cfg["parallelism"] = "single GPU"
     cfg["l2"] = "inputs larger than L2 (no flush)" if args.workload != "tiny" else "inputs fit in L2"
+    cfg["launch"] = ("timed steps replay a CUDA graph of the step's launches" if world == 1 and not args.no_graph
+                     else "eager launches")
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
