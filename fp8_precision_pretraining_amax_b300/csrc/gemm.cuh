@@ -18,8 +18,8 @@
 //   warp 0      operand producer (both CTAs): TMA loads of this CTA's 128
 //               rows of A and its half (128 rows) of B per chunk into a
 //               5-stage shared-memory ring (128-byte swizzle), completion
-//               bytes counted on the even CTA's full barrier, which expects
-//               both CTAs' bytes.
+//               bytes counted on the even CTA's full barrier, which the even
+//               producer arms for both CTAs' bytes.
 //   warp 2      scale producer (both CTAs): bulk and cp.async copies of each
 //               chunk's scales (this CTA's 128 row scales and the tile's
 //               column scales) into a 6-slot ring, so no promotion warp ever
@@ -32,16 +32,20 @@
 //               producers may refill the stage) and partial-full barriers.
 //   warp 3      idle (the first warpgroup gives up registers: 40 per thread)
 //   warps 4..11 promotion (two warpgroups at 232 registers per thread, both
-//               CTAs): each thread owns one output row and 128 columns; it
-//               reads the chunk partial from its CTA's TMEM (tcgen05.ld),
+//               CTAs): each warp owns the 32 TMEM lanes (rows) of its SM
+//               sub-partition and 128 of the tile's columns, 128 FP32
+//               accumulators per thread (Fprop/Dgrad: one row and 128
+//               columns; Wgrad: four rows and 32 columns, see load_group).
+//               It reads the chunk partial from its CTA's TMEM (tcgen05.ld),
 //               hands the buffer back to the MMA (the even CTA's
 //               partial-empty barrier, 16 arrivals: 8 warps per CTA) as soon
 //               as the partial is in registers, and multiplies it by the
-//               chunk's scale product into FP32 accumulators.  While it does
+//               chunk's scale product into the accumulators.  While it does
 //               so the tensor cores already compute the next chunk into the
 //               other buffer.  After the last chunk the accumulators are
 //               rounded to BF16 (or kept in FP32 and optionally added into
 //               the output with a TMA reduce) and stored with TMA.
+// Odd-numbered tiles of a cluster walk the reduction backwards (chunk_of).
 // Per SM and chunk this moves 32 KB through TMA and shared memory (a single
 // CTA with a 128 x 256 tile needs 48 KB) for the same tensor-core work.
 // Every wait is bounded: a stalled pipeline records FP8BQ_ERR_TIMEOUT in the
