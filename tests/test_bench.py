@@ -120,3 +120,32 @@ def test_data_parallel_plan_all_reduces_the_fp32_wgrad():
         assert kinds[i + 1] == "comm_allreduce_dw"
         assert u.outputs[-1].dtype == torch.float32
     assert sum(k.startswith("gemm") for u in units for k, _, _ in u.launches) == 12
+
+
+@pytest.mark.parametrize("workload,world,variant", [("layer_3p8b", 1, "fp32-scale"), ("layer_3p8b", 2, "fp32-scale"),
+                                                    ("layer_3p8b", 1, "mx"), ("swiglu", 1, "fp32-scale"),
+                                                    ("up_bwd", 1, "fp32-scale"), ("qkv_1p7b", 1, "fp32-scale")])
+def test_end_to_end_copy_schedule_points_at_the_right_launches(workload, world, variant):
+    """The end-to-end leg copies an input in once its previous reader ran and
+    an output out once its producer ran: every input's readers are the
+    quantizers that consume it, and every output is ready after the GEMM (or
+    all-reduce) that writes it."""
+    from fp8_precision_pretraining_amax_b300 import fp8bq
+    shapes = bench.workload_shapes(workload, tokens=256)
+    lins = [_Lin(n, M, K, N) for n, M, K, N in shapes]
+    units = bench.build_units(fp8bq, workload, lins, "cpu", world, variant)
+    for u in units:
+        kinds = [k for k, _, _ in u.launches]
+        assert len(u.reads) == len(u.inputs) and len(u.ready) == len(u.outputs)
+        for first, last in u.reads:
+            assert first <= last and kinds[first].startswith("quant") and kinds[last].startswith("quant")
+        if u.name == "weights" or workload != "layer_3p8b":
+            continue
+        fprop, dgrad = ("gemm_mx_fprop", "gemm_mx_dgrad") if variant == "mx" else ("gemm_fprop", "gemm_dgrad")
+        y, dx, dw = u.ready
+        assert kinds[y] == fprop and kinds[dx] == dgrad and dw == len(kinds) - 1
+        assert kinds[dw] == ("comm_allreduce_dw" if world > 1 else kinds[dw])
+        # X is read by the pass that quantizes it, dY by the pass over dY, before the GEMMs that need them
+        x_first = u.reads[0][0]
+        dy_first = u.reads[-1][0]
+        assert x_first < y and dy_first < dx
