@@ -132,7 +132,7 @@ constexpr size_t kGemmSmemBytes =
     1024 + kStages * (kStageBytesA + kStageBytesB) + kPromoWarps * kEpiWarpBytes + sizeof(GemmCtl);
 static_assert(kGemmSmemBytes <= 232448, "more dynamic shared memory than one sm_103 CTA can have");
 
-// One lane waits, the verdict is broadcast so the warp stays converged.
+// One lane waits, the result is broadcast so the warp stays converged.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           uint64_t limit_ns) {
     int ok = 0;
