@@ -285,7 +285,8 @@ def step_launches(fp8bq, L, lin):
         ("quant_rowcol", rowcol_bytes(M, N),
          lambda: fp8bq.fp8bq_quantize_rowcol(lin.dy, L.dyq, L.sdy, L.dyqT, L.sdyT)),
         ("gemm_dgrad", 2 * M * N * K, lambda: fp8bq.fp8bq_gemm_dgrad(L.dyq, L.sdy, L.wqT, L.sw, L.dx)),
-        ("gemm_wgrad", 2 * M * N * K, lambda: fp8bq.fp8bq_gemm_wgrad(L.dyqT, L.sdyT, L.xqT, L.sxT, L.dw)),
+        ("gemm_wgrad", 2 * M * N * K,
+         lambda: fp8bq.fp8bq_gemm_wgrad_balanced(L.dyqT, L.sdyT, L.xqT, L.sxT, L.dw, L.wscratch)),
     ]
 
 
@@ -405,7 +406,8 @@ def build_units(fp8bq, name, lins, dev, world, variant="fp32-scale"):
             ("quant_rowcol", rowcol_bytes(M, N),
              lambda: fp8bq.fp8bq_quantize_rowcol(lin.dy, L.dyq, L.sdy, L.dyqT, L.sdyT)),
             ("gemm_dgrad", 2 * M * N * K, lambda: fp8bq.fp8bq_gemm_dgrad(L.dyq, L.sdy, L.wqT, L.sw, L.dx)),
-            ("gemm_wgrad", 2 * M * N * K, lambda: fp8bq.fp8bq_gemm_wgrad(L.dyqT, L.sdyT, L.xqT, L.sxT, L.dw)),
+            ("gemm_wgrad", 2 * M * N * K,
+             lambda: fp8bq.fp8bq_gemm_wgrad_balanced(L.dyqT, L.sdyT, L.xqT, L.sxT, L.dw, L.wscratch)),
         ]
         dw = data_parallel_wgrad(fp8bq, L, launches, dist) if world > 1 else L.dw
         # the weight's codes (and transposed codes) come from the forward pass

@@ -109,6 +109,8 @@ fp8bq_status probe_device(DeviceState** out) {
                 cudaFuncSetAttribute(fp8bq::gemm_block_scaled_kernel<fp8bq::kModeDgrad>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
                 cudaFuncSetAttribute(fp8bq::gemm_block_scaled_kernel<fp8bq::kModeWgrad>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+                cudaFuncSetAttribute(fp8bq::gemm_block_scaled_kernel<fp8bq::kModeWgrad, true>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
                 return FP8BQ_ERR_CUDA;
             if (set_tile_smem<false>() != cudaSuccess || set_tile_smem<true>() != cudaSuccess) return FP8BQ_ERR_CUDA;
@@ -267,7 +269,19 @@ struct GemmOut {
     bool accumulate = false;
     uint8_t* q = nullptr;
     float* sq = nullptr;
+    uint8_t* scratch = nullptr;   // balanced order's split slots and counters (null: tile order)
+    int64_t scratch_bytes = 0;
 };
+
+// Scratch of the balanced order for `pairs` clusters: one arrival counter per
+// boundary, CTA rank and promotion warp (rounded up to 256 bytes), then the
+// boundaries' split slots.
+int64_t split_counter_bytes(int pairs) {
+    return ((static_cast<int64_t>(pairs - 1) * fp8bq::kSplitBoundaryCounters * 4 + 255) / 256) * 256;
+}
+int64_t split_scratch_bytes(int pairs) {
+    return pairs < 2 ? 0 : split_counter_bytes(pairs) + static_cast<int64_t>(pairs - 1) * fp8bq::kSplitBoundaryBytes;
+}
 
 // n FP32 values set to v (scales of all-zero tiles).
 __global__ void fill_f32_kernel(float* p, int64_t n, float v) {
@@ -326,6 +340,7 @@ fp8bq_status run_gemm(const uint8_t* A, const float* sA, const uint8_t* B, const
     DeviceState* dev = nullptr;
     fp8bq_status st = probe_device(&dev);
     if (st != FP8BQ_OK) return st;
+    if (o.scratch != nullptr && o.scratch_bytes < split_scratch_bytes(dev->max_pairs)) return FP8BQ_ERR_SHAPE;
     if (Kr == 0) {
         // empty reduction: the product is exactly zero (adding it changes
         // nothing); its tiles quantize to +0 codes with scale 1
@@ -367,12 +382,36 @@ fp8bq_status run_gemm(const uint8_t* A, const float* sA, const uint8_t* B, const
     p.timeout_ns = kDefaultTimeoutNs;
     // persistent: one CTA pair per TPC that can hold one, never more pairs than tiles
     const int pairs = static_cast<int>(tiles < dev->max_pairs ? tiles : dev->max_pairs);
+    // balanced order (with scratch): every cluster gets an equal share of the
+    // chunks; it needs at least one whole tile per cluster (tiles >= pairs,
+    // always true here) and two clusters to share anything
+    p.split_ws = nullptr;
+    p.split_cnt = nullptr;
+    // balanced order: only Wgrad offers it, its chunk count must fit the
+    // kernel's 32-bit share arithmetic, and it is used where whole-tile rounds
+    // would leave at least 10 % of the clusters' time idle in the last round
+    // (it costs about 5 % per chunk: the clusters no longer walk their tiles
+    // in step, so concurrent tiles share fewer operand chunks in L2)
+    const int64_t rounds = (tiles + pairs - 1) / pairs;
+    const bool balanced = MODE == fp8bq::kModeWgrad && o.scratch != nullptr && pairs >= 2 &&
+                          tiles * p.KC < (int64_t(1) << 31) && 10 * (rounds * pairs - tiles) >= rounds * pairs;
+    if (balanced) {
+        p.split_cnt = reinterpret_cast<unsigned int*>(o.scratch);
+        p.split_ws = reinterpret_cast<float*>(o.scratch + split_counter_bytes(pairs));
+    }
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     gemm_launch_config(&cfg, attr, pairs, stream);
-    if (cudaLaunchKernelEx(&cfg, fp8bq::gemm_block_scaled_kernel<MODE>, ta, tb, td, tq, p, dev->status) !=
-        cudaSuccess)
-        return FP8BQ_ERR_CUDA;
+    cudaError_t e;
+    if constexpr (MODE == fp8bq::kModeWgrad) {
+        if (balanced)
+            e = cudaLaunchKernelEx(&cfg, fp8bq::gemm_block_scaled_kernel<MODE, true>, ta, tb, td, tq, p, dev->status);
+        else
+            e = cudaLaunchKernelEx(&cfg, fp8bq::gemm_block_scaled_kernel<MODE>, ta, tb, td, tq, p, dev->status);
+    } else {
+        e = cudaLaunchKernelEx(&cfg, fp8bq::gemm_block_scaled_kernel<MODE>, ta, tb, td, tq, p, dev->status);
+    }
+    if (e != cudaSuccess) return FP8BQ_ERR_CUDA;
     return launch_status();
 }
 
@@ -568,6 +607,29 @@ fp8bq_status fp8bq_gemm_wgrad(const uint8_t* dyqT, const float* sdyT, const uint
     if (dw == nullptr && N > 0 && K > 0) return FP8BQ_ERR_NULL;
     GemmOut o;
     o.d = dw;
+    return run_gemm<fp8bq::kModeWgrad>(dyqT, sdyT, xqT, sxT, o, N, K, M, reinterpret_cast<cudaStream_t>(stream));
+}
+
+fp8bq_status fp8bq_gemm_wgrad_scratch_bytes(int64_t* bytes) {
+    if (bytes == nullptr) return FP8BQ_ERR_NULL;
+    DeviceState* dev = nullptr;
+    fp8bq_status st = probe_device(&dev);
+    if (st != FP8BQ_OK) return st;
+    *bytes = split_scratch_bytes(dev->max_pairs);
+    return FP8BQ_OK;
+}
+
+fp8bq_status fp8bq_gemm_wgrad_balanced(const uint8_t* dyqT, const float* sdyT, const uint8_t* xqT, const float* sxT,
+                                       uint16_t* dw, int64_t M, int64_t N, int64_t K, void* scratch,
+                                       int64_t scratch_bytes, fp8bq_stream_t stream) {
+    if (dw == nullptr && N > 0 && K > 0) return FP8BQ_ERR_NULL;
+    if (scratch == nullptr) return FP8BQ_ERR_NULL;
+    if (!aligned16(scratch)) return FP8BQ_ERR_ALIGN;
+    if (scratch_bytes < 0) return FP8BQ_ERR_SHAPE;
+    GemmOut o;
+    o.d = dw;
+    o.scratch = static_cast<uint8_t*>(scratch);
+    o.scratch_bytes = scratch_bytes;
     return run_gemm<fp8bq::kModeWgrad>(dyqT, sdyT, xqT, sxT, o, N, K, M, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -80,6 +80,12 @@ constexpr int kPromoWarps = 8;
 constexpr uint32_t kStageBytesA = kBM * kBK;
 constexpr uint32_t kStageBytesB = kBNHalf * kBK;
 constexpr uint32_t kTmemCols = 2 * kBN;
+// Balanced order: one promotion warp's accumulators (32 threads x 128 floats)
+// in a split slot, and the slots' and counters' sizes per boundary between
+// two clusters (2 parts x 2 CTA ranks x 8 warps).
+constexpr int64_t kSplitSliceFloats = 32 * 128;
+constexpr int64_t kSplitBoundaryBytes = 2 * 2 * kPromoWarps * kSplitSliceFloats * 4;
+constexpr int64_t kSplitBoundaryCounters = 2 * kPromoWarps;
 // Epilogue staging: a promotion warp writes its 32 rows x 128 BF16 columns
 // as four 32 x 32 boxes (64-byte rows, 64-byte swizzle) through three 2 KB
 // staging boxes used in rotation, so a box is written while the TMA stores
@@ -100,6 +106,8 @@ struct GemmParams {
     int out_bf16;         // BF16 D is written (may be 0 when only codes are wanted)
     int out_q;            // also quantize the BF16-rounded output per 1x128 row tile
     float* sq;            // out_q: output scales [J/128][I]
+    float* split_ws;      // balanced order: partial accumulators of split tiles
+    unsigned int* split_cnt;  // balanced order: arrival counters (boundary, CTA rank, warp)
     uint64_t timeout_ns;
 };
 
@@ -159,6 +167,46 @@ __device__ __forceinline__ bool warp_wait_backoff(uint64_t* bar, uint32_t parity
 // the same bound (any order of the FP32 sum over chunks is a valid reading).
 __device__ __forceinline__ int chunk_of(int i, int it, int KC) { return (it & 1) ? KC - 1 - i : i; }
 
+// Balanced order (the kBal kernels, Wgrad with scratch): cluster cid of n
+// takes the equal share [U cid / n, U (cid + 1) / n) of all U = num_tiles *
+// KC chunks in tile-major order (U < 2^31), so no cluster idles in a last,
+// partly filled wave of long tiles.  With num_tiles >= n every share holds
+// at least one tile's worth of chunks, so a tile is split between at most two
+// neighbouring clusters: its first chunks end cluster b's share ("part 0"),
+// the rest begin cluster b + 1's ("part 1"); b names the split.
+struct BalIter {
+    int u, u_end;
+};
+
+__device__ __forceinline__ BalIter bal_init(const GemmParams& p, int cid, int ncl) {
+    const int64_t U = static_cast<int64_t>(p.num_tiles) * p.KC;
+    return BalIter{static_cast<int>(U * cid / ncl), static_cast<int>(U * (cid + 1) / ncl)};
+}
+
+// The next segment of the share: chunks [c_lo, c_hi) of tile; false at its end.
+__device__ __forceinline__ bool bal_next(BalIter& b, const GemmParams& p, int& tile, int& c_lo, int& c_hi) {
+    if (b.u >= b.u_end) return false;
+    tile = b.u / p.KC;
+    c_lo = b.u - tile * p.KC;
+    c_hi = min(p.KC, c_lo + (b.u_end - b.u));
+    b.u += c_hi - c_lo;
+    return true;
+}
+
+// Segment k of cluster cid's balanced share, recomputed from scratch (no
+// state carried between segments): false when the share has no segment k.
+__device__ __forceinline__ bool bal_segment(const GemmParams& p, int cid, int ncl, int k, int& tile, int& c_lo,
+                                            int& c_hi) {
+    const BalIter b = bal_init(p, cid, ncl);
+    const int t = b.u / p.KC + k;
+    const int lo = max(b.u, t * p.KC), hi = min(b.u_end, (t + 1) * p.KC);
+    if (lo >= hi) return false;
+    tile = t;
+    c_lo = lo - t * p.KC;
+    c_hi = hi - t * p.KC;
+    return true;
+}
+
 // Stop both CTAs of the pair and record the timeout.
 __device__ __forceinline__ void raise_abort(GemmCtl* ctl, uint32_t peer_abort, unsigned int* status) {
     if ((threadIdx.x & 31) == 0) {
@@ -190,7 +238,7 @@ __device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
 __device__ __forceinline__ void cp_async_drain() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Launched as clusters of two CTAs (grid = 2 x clusters).
-template <int MODE>
+template <int MODE, bool kBal = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_block_scaled_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmQ,
@@ -258,13 +306,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t full0 = mapa_shared(smem_addr(&ctl->full[0]), 0);
         uint32_t s = 0, ph = 0, issued = 0;
         bool ok = true;
-        int it = 0;
-        for (int tile = first_tile; tile < p.num_tiles && ok; tile += tile_step, ++it) {
+        int it = -1, tile = first_tile - tile_step, c_lo = 0, c_hi = p.KC;
+        BalIter bi = bal_init(p, first_tile, tile_step);
+        while (ok) {
+            if constexpr (kBal) {
+                if (!bal_next(bi, p, tile, c_lo, c_hi)) break;
+            } else {
+                tile += tile_step;
+                if (tile >= p.num_tiles) break;
+            }
+            ++it;
             const int tm = tile / p.tiles_n, tn = tile - tm * p.tiles_n;
             const int r0 = tm * kPairM + static_cast<int>(rank) * kBM;  // this CTA's first row
             const int b0 = tn * kBN + static_cast<int>(rank) * kBNHalf;  // this CTA's first B row
-            for (int i = 0; i < p.KC; ++i) {
-                const int c = chunk_of(i, it, p.KC);
+            for (int i = c_lo; i < c_hi; ++i) {
+                const int c = kBal ? i : chunk_of(i, it, p.KC);
                 if (!warp_wait(&ctl->empty[s], ph ^ 1, abort_flag, lim)) { ok = false; break; }
                 if (lane == 0) {
                     if (leader) mbar_arrive_expect_tx(&ctl->full[s], 2 * (kStageBytesA + kStageBytesB));
@@ -287,15 +343,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // the problem are skipped.
         uint32_t q = 0, qph = 0, issued = 0;
         bool ok = true;
-        int it = 0;
-        for (int tile = first_tile; tile < p.num_tiles && ok; tile += tile_step, ++it) {
+        int it = -1, tile = first_tile - tile_step, c_lo = 0, c_hi = p.KC;
+        BalIter bi = bal_init(p, first_tile, tile_step);
+        while (ok) {
+            if constexpr (kBal) {
+                if (!bal_next(bi, p, tile, c_lo, c_hi)) break;
+            } else {
+                tile += tile_step;
+                if (tile >= p.num_tiles) break;
+            }
+            ++it;
             const int tm = tile / p.tiles_n, tn = tile - tm * p.tiles_n;
             const int r0 = tm * kPairM + static_cast<int>(rank) * kBM;
             const int j0 = tn * kBN;
             const uint32_t a_bytes = r0 < p.I ? 128u * 4u : 0u;
             const uint32_t b_bytes = MODE == kModeWgrad ? static_cast<uint32_t>(min(p.J - j0, kBN)) * 4u : 0u;
-            for (int i = 0; i < p.KC; ++i) {
-                const int c = chunk_of(i, it, p.KC);
+            for (int i = c_lo; i < c_hi; ++i) {
+                const int c = kBal ? i : chunk_of(i, it, p.KC);
                 if (!warp_wait_backoff(&ctl->sempty[q], qph ^ 1, abort_flag, lim)) { ok = false; break; }
                 ScaleSlot& sl = ctl->scl[q];
                 if (lane == 0) {
@@ -327,8 +391,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_e4m3_f32(kPairM, kBN);
             uint32_t s = 0, ph = 0, buf = 0, tph = 0;
-            for (int tile = first_tile; tile < p.num_tiles && ok; tile += tile_step) {
-                for (int c = 0; c < p.KC; ++c) {
+            // balanced: the MMAs need no tile boundaries, one flat loop
+            const BalIter bi = bal_init(p, first_tile, tile_step);
+            const int n_outer = kBal ? 1 : p.num_tiles;
+            const int n_inner = kBal ? bi.u_end - bi.u : p.KC;
+            for (int tile = kBal ? 0 : first_tile; tile < n_outer && ok; tile += kBal ? 1 : tile_step) {
+                for (int c = 0; c < n_inner; ++c) {
                     // Both waits suspend (try_wait): this thread shares its SM
                     // sub-partition with two promotion warps (TMEM lanes 32-63),
                     // the last to hand the partial buffer back, so it must not
@@ -369,7 +437,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         uint32_t buf = 0, tph = 0, q = 0, qph = 0;
         int nbox = 0;   // staging box of the next BF16 output box
         bool ok = true;
-        for (int tile = first_tile; tile < p.num_tiles && ok; tile += tile_step) {
+        int tile = first_tile - tile_step, c_lo = 0, c_hi = p.KC;
+        for (int seg = 0; ok; ++seg) {
+            if constexpr (kBal) {
+                if (!bal_segment(p, first_tile, tile_step, seg, tile, c_lo, c_hi)) break;
+            } else {
+                tile += tile_step;
+                if (tile >= p.num_tiles) break;
+            }
             const int tm = tile / p.tiles_n, tn = tile - tm * p.tiles_n;
             const int r0 = tm * kPairM + static_cast<int>(rank) * kBM;  // first row of this CTA's half
             const bool rv = r0 < p.I;
@@ -379,7 +454,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
             for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
 
-            for (int c = 0; c < p.KC; ++c) {
+            for (int c = c_lo; c < c_hi; ++c) {
                 if (!warp_wait(&ctl->sfull[q], qph, abort_flag, lim)) { ok = false; break; }
                 const ScaleSlot& sl = ctl->scl[q];
                 const float sab = MODE == kModeWgrad ? 0.0f : sl.a[row] * sl.b[half];
@@ -465,6 +540,44 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 if (buf == 0) tph ^= 1;
             }
             if (!ok) break;
+            if constexpr (kBal) {
+                if (c_lo > 0 || c_hi < p.KC) {
+                    // A tile split between two clusters (see BalIter): each part
+                    // leaves its partial accumulators in the split slot of its
+                    // boundary, then counts itself in; the part that arrives
+                    // second adds the other's partial to its own (FP32 addition
+                    // commutes: the sum does not depend on the order of
+                    // arrival) and writes the tile.  Warp-sized slices: warp pw
+                    // of either part holds the same rows and columns.
+                    const int part = c_lo == 0 ? 0 : 1;
+                    const int bnd = part == 0 ? first_tile : first_tile - 1;
+                    float* mine = p.split_ws +
+                                  ((static_cast<int64_t>(bnd) * 2 + part) * 2 + rank) * kSplitSliceFloats * kPromoWarps +
+                                  static_cast<int64_t>(pw) * kSplitSliceFloats;
+                    const float* other = mine + (part == 0 ? 2 : -2) * kSplitSliceFloats * kPromoWarps;
+#pragma unroll
+                    for (int i4 = 0; i4 < 32; ++i4)
+                        *reinterpret_cast<float4*>(mine + (i4 * 32 + lane) * 4) =
+                            make_float4(acc[4 * i4], acc[4 * i4 + 1], acc[4 * i4 + 2], acc[4 * i4 + 3]);
+                    __threadfence();
+                    __syncwarp();
+                    unsigned int* cnt = p.split_cnt + (bnd * 2 + static_cast<int>(rank)) * kPromoWarps + pw;
+                    unsigned int arrived = 0;
+                    if (lane == 0) arrived = atomicAdd(cnt, 1u);
+                    arrived = __shfl_sync(0xFFFFFFFFu, arrived, 0);
+                    if (arrived == 0) continue;   // the other part completes the tile
+                    __threadfence();
+#pragma unroll
+                    for (int i4 = 0; i4 < 32; ++i4) {
+                        const float4 o = __ldcg(reinterpret_cast<const float4*>(other + (i4 * 32 + lane) * 4));
+                        acc[4 * i4] = __fadd_rn(acc[4 * i4], o.x);
+                        acc[4 * i4 + 1] = __fadd_rn(acc[4 * i4 + 1], o.y);
+                        acc[4 * i4 + 2] = __fadd_rn(acc[4 * i4 + 2], o.z);
+                        acc[4 * i4 + 3] = __fadd_rn(acc[4 * i4 + 3], o.w);
+                    }
+                    if (lane == 0) *cnt = 0u;   // zero again for the next launch
+                }
+            }
             // Epilogue: round to BF16 (or keep FP32) into this warp's swizzled
             // staging box, then one lane issues the TMA store or reduce-add
             // (asynchronous: the last one drains while the next tile's chunks

@@ -37,6 +37,14 @@ class LinearFP8:
         self.dyqT, self.sdyT = e(N, M, dt=u8), e(M // 128, N, dt=f32)
         self.xqT, self.sxT = e(K, M, dt=u8), e(M // 128, K, dt=f32)
         self.y, self.dx, self.dw = e(M, N, dt=bf), e(M, K, dt=bf), e(N, K, dt=bf)
+        self._wscratch = None
+
+    @property
+    def wscratch(self) -> torch.Tensor:
+        """This layer's scratch for the balanced Wgrad (zeroed once, left zero by every call)."""
+        if self._wscratch is None:
+            self._wscratch = fp8bq.wgrad_scratch(self.dw.device)
+        return self._wscratch
 
     @property
     def flops_per_gemm(self) -> int:
@@ -57,7 +65,7 @@ class LinearFP8:
         """Needs forward(for_backward=True) first (wqT, sw, xqT, sxT are reused)."""
         fp8bq.fp8bq_quantize_rowcol(dy, self.dyq, self.sdy, self.dyqT, self.sdyT)
         fp8bq.fp8bq_gemm_dgrad(self.dyq, self.sdy, self.wqT, self.sw, self.dx)
-        fp8bq.fp8bq_gemm_wgrad(self.dyqT, self.sdyT, self.xqT, self.sxT, self.dw)
+        fp8bq.fp8bq_gemm_wgrad_balanced(self.dyqT, self.sdyT, self.xqT, self.sxT, self.dw, self.wscratch)
         return self.dx, self.dw
 
     def step(self, x: torch.Tensor, w: torch.Tensor, dy: torch.Tensor):

@@ -243,6 +243,41 @@ fp8bq_status fp8bq_gemm_wgrad(const uint8_t* dyqT, const float* sdyT, const uint
                               uint16_t* dw, int64_t M, int64_t N, int64_t K, fp8bq_stream_t stream);
 
 /*
+ * Wgrad, balanced work split: the same product as fp8bq_gemm_wgrad, with
+ * every cluster of the persistent grid taking an equal share of all tiles'
+ * reduction chunks instead of whole tiles, so no cluster idles in a last,
+ * partly filled wave of tiles (each Wgrad tile reduces over all M tokens, so
+ * such a wave costs a whole tile's time).  The split is used where whole-tile
+ * rounds would leave at least 10 % of the grid's time idle; otherwise the
+ * call runs fp8bq_gemm_wgrad's tile order (scratch untouched).  A tile split between two
+ * neighbouring clusters is completed by the one that finishes second: it
+ * adds the other's FP32 partial, left in `scratch`, to its own (FP32
+ * addition commutes, so the result does not depend on which finishes first
+ * and is the same on every call).  The result differs from
+ * fp8bq_gemm_wgrad's only in the grouping of the FP32 sum over chunks on
+ * split tiles: within the same acceptance bound.
+ *   scratch        device buffer of at least scratch_bytes bytes, 16-byte
+ *                  aligned, all zero before its first use; every completed
+ *                  call leaves it ready for the next (the arrival counters at
+ *                  its start back at zero; the rest holds no state between
+ *                  calls).  Calls that share a scratch buffer must not
+ *                  overlap in time (order them on one stream).  After
+ *                  FP8BQ_ERR_TIMEOUT, zero it again.
+ *   scratch_bytes  at least fp8bq_gemm_wgrad_scratch_bytes() for the
+ *                  current device (else FP8BQ_ERR_SHAPE)
+ * Other arguments and requirements as fp8bq_gemm_wgrad.
+ * Source: none in the pages; a scheduling form of the Wgrad GEMM of the
+ *   Puro-2B technical report (lkr-homepage blog), section 2 "FP8".
+ */
+fp8bq_status fp8bq_gemm_wgrad_balanced(const uint8_t* dyqT, const float* sdyT, const uint8_t* xqT, const float* sxT,
+                                       uint16_t* dw, int64_t M, int64_t N, int64_t K, void* scratch,
+                                       int64_t scratch_bytes, fp8bq_stream_t stream);
+
+/* Bytes of scratch fp8bq_gemm_wgrad_balanced needs on the current device
+ * (the same for every shape; 0 when the device runs a single cluster). */
+fp8bq_status fp8bq_gemm_wgrad_scratch_bytes(int64_t* bytes);
+
+/*
  * Wgrad with an FP32 output, for keeping weight gradients in FP32 across
  * micro-batches and data-parallel ranks (the Puro-2B report keeps training
  * state in FP32, section 2 "FP8").  Same operands and product as

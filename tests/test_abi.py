@@ -127,6 +127,16 @@ def test_fused_and_fp32_entry_points_reject_bad_arguments_on_the_host(lib):
     assert wf(P, P, P, P, P, 100, 128, 128, 0, None) == ERR_SHAPE
     assert wf(P, P, P, P, None, 128, 128, 128, 1, None) == ERR_NULL
     assert wf(P, P, P, P, P + 8, 128, 128, 128, 0, None) == ERR_ALIGN
+    wb = lib.fp8bq_gemm_wgrad_balanced
+    wb.restype, wb.argtypes = i32, [vp] * 5 + [i64] * 3 + [vp, i64, vp]
+    assert wb(P, P, P, P, P, 128, 128, 128, None, 1 << 30, None) == ERR_NULL   # scratch required
+    assert wb(P, P, P, P, P, 128, 128, 128, P + 4, 1 << 30, None) == ERR_ALIGN
+    assert wb(P, P, P, P, P, 128, 128, 128, P, -1, None) == ERR_SHAPE
+    assert wb(P, P, P, P, P, 100, 128, 128, P, 1 << 30, None) == ERR_SHAPE      # M not a multiple of 128
+    assert wb(P, P, P, P, None, 128, 128, 128, P, 1 << 30, None) == ERR_NULL
+    sb = lib.fp8bq_gemm_wgrad_scratch_bytes
+    sb.restype, sb.argtypes = i32, [vp]
+    assert sb(None) == ERR_NULL
     fq = lib.fp8bq_gemm_fprop_q
     fq.restype, fq.argtypes = i32, [vp] * 7 + [i64] * 3 + [vp]
     assert fq(P, P, P, P, None, None, P, 128, 128, 128, None) == ERR_NULL   # codes required

@@ -302,3 +302,53 @@ def test_fprop_q_empty_reduction(fb):
                           None, yq, sy)
     fb.check()
     assert torch.all(yq == 0) and torch.all(sy == 1.0)
+
+
+def _split_counter_bytes(fb):
+    """Bytes of the balanced Wgrad's arrival counters at the start of its
+    scratch (one 4-byte counter per CTA rank and promotion warp, 16 per
+    boundary between two clusters; each boundary also has 512 KB of slots)."""
+    total = fb.fp8bq_gemm_wgrad_scratch_bytes()
+    return (total // (512 * 1024 + 64)) * 64
+
+
+def test_wgrad_balanced_splits_tiles_and_repeats_bit_for_bit(fb):
+    """81 output tiles of 256 x 256, 16 chunks each, over the persistent
+    grid's clusters: most clusters' equal shares of the chunks end inside a
+    tile, which the two neighbours then complete together.  Every output
+    tile is within the bound, a second call gives the same bits, and the
+    arrival counters are back at zero."""
+    rng = np.random.default_rng(29)
+    M, N, K = 2048, 2304, 2304
+    dyqT, xqT = random_codes(rng, (N, M)), random_codes(rng, (K, M))
+    sdyT, sxT = random_scales(rng, (M // 128, N)), random_scales(rng, (M // 128, K))
+    dev = [to_dev(a) for a in (dyqT, sdyT, xqT, sxT)]
+    scratch = fb.wgrad_scratch(dev[0].device)
+    dw1 = torch.empty((N, K), dtype=torch.bfloat16, device="cuda")
+    dw2 = torch.empty_like(dw1)
+    fb.fp8bq_gemm_wgrad_balanced(*dev, dw1, scratch)
+    fb.fp8bq_gemm_wgrad_balanced(*dev, dw2, scratch)
+    fb.check()
+    torch.cuda.synchronize()
+    assert torch.equal(dw1.view(torch.int16), dw2.view(torch.int16))
+    nc = _split_counter_bytes(fb)
+    assert nc > 0 and int(scratch[:nc].sum()) == 0
+    check_gemm_tiles(dw1, oracle.gemm_wgrad_mm, (dyqT, sdyT, xqT, sxT), _all_tiles(N, K), what="wgrad balanced")
+
+
+def test_wgrad_balanced_exact_integer_case_is_bit_exact(fb):
+    """Small integers and power-of-two scales: every partial sum is exact in
+    FP32 however the chunks are grouped, so the balanced split must give the
+    oracle's rounding bit for bit, split tiles included."""
+    rng = np.random.default_rng(31)
+    M, N, K = 1024, 2304, 2304
+    dyqT, _ = _integer_operands(rng, (N, M))
+    xqT, _ = _integer_operands(rng, (K, M))
+    sdyT = np.exp2(rng.integers(-2, 3, size=(M // 128, N))).astype(np.float32)
+    sxT = np.exp2(rng.integers(-2, 3, size=(M // 128, K))).astype(np.float32)
+    scratch = fb.wgrad_scratch(torch.device("cuda"))
+    dw = torch.empty((N, K), dtype=torch.bfloat16, device="cuda")
+    fb.fp8bq_gemm_wgrad_balanced(to_dev(dyqT), to_dev(sdyT), to_dev(xqT), to_dev(sxT), dw, scratch)
+    fb.check()
+    exact, _ = oracle.gemm_wgrad_mm(dyqT, sdyT, xqT, sxT)
+    assert np.array_equal(synth.bf16_bits(dw), oracle.bf16_from_double(exact))
