@@ -23,6 +23,17 @@ __device__ unsigned int g_status_word;
 // Where fp8bq_check's exchange kernel leaves the word it took.
 __device__ unsigned int g_status_taken;
 
+// Scratch of fp8bq_gemm_wgrad_balanced_static, in the module's own device
+// memory (no allocation call): the balanced Wgrad's counters and split slots
+// for up to 74 clusters, the CTA pairs of a 148-SM B300 (devices that run
+// more are refused).  Zero at module load; every completed call leaves the
+// counters zero again.
+constexpr int kStaticScratchPairs = 74;
+constexpr int64_t kStaticScratchBytes =
+    ((static_cast<int64_t>(kStaticScratchPairs - 1) * fp8bq::kSplitBoundaryCounters * 4 + 255) / 256) * 256 +
+    static_cast<int64_t>(kStaticScratchPairs - 1) * fp8bq::kSplitBoundaryBytes;
+static __device__ __align__(256) uint8_t g_wgrad_scratch[kStaticScratchBytes];
+
 // Reads the status word and clears it in one atomic step, so a timeout that
 // a kernel on another stream records meanwhile is either taken now or stays
 // for the next check.
@@ -40,6 +51,7 @@ struct DeviceState {
     int max_pairs = 0;               // co-resident GEMM clusters (CTA pairs)
     unsigned int* status = nullptr;  // device address of g_status_word
     unsigned int* taken = nullptr;   // device address of g_status_taken
+    uint8_t* wgrad_scratch = nullptr;  // device address of g_wgrad_scratch
     std::mutex check_mu;             // one fp8bq_check at a time uses `taken`
 };
 
@@ -103,6 +115,8 @@ fp8bq_status probe_device(DeviceState** out) {
             d.status = static_cast<unsigned int*>(p);
             if (cudaGetSymbolAddress(&p, g_status_taken) != cudaSuccess) return FP8BQ_ERR_CUDA;
             d.taken = static_cast<unsigned int*>(p);
+            if (cudaGetSymbolAddress(&p, g_wgrad_scratch) != cudaSuccess) return FP8BQ_ERR_CUDA;
+            d.wgrad_scratch = static_cast<uint8_t*>(p);
             const int smem = static_cast<int>(fp8bq::kGemmSmemBytes);
             if (cudaFuncSetAttribute(fp8bq::gemm_block_scaled_kernel<fp8bq::kModeFprop>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
@@ -630,6 +644,21 @@ fp8bq_status fp8bq_gemm_wgrad_balanced(const uint8_t* dyqT, const float* sdyT, c
     o.d = dw;
     o.scratch = static_cast<uint8_t*>(scratch);
     o.scratch_bytes = scratch_bytes;
+    return run_gemm<fp8bq::kModeWgrad>(dyqT, sdyT, xqT, sxT, o, N, K, M, reinterpret_cast<cudaStream_t>(stream));
+}
+
+fp8bq_status fp8bq_gemm_wgrad_balanced_static(const uint8_t* dyqT, const float* sdyT, const uint8_t* xqT,
+                                              const float* sxT, uint16_t* dw, int64_t M, int64_t N, int64_t K,
+                                              fp8bq_stream_t stream) {
+    if (dw == nullptr && N > 0 && K > 0) return FP8BQ_ERR_NULL;
+    DeviceState* dev = nullptr;
+    fp8bq_status st = probe_device(&dev);
+    if (st != FP8BQ_OK) return st;
+    if (split_scratch_bytes(dev->max_pairs) > kStaticScratchBytes) return FP8BQ_ERR_SHAPE;  // more clusters than it holds
+    GemmOut o;
+    o.d = dw;
+    o.scratch = dev->wgrad_scratch;
+    o.scratch_bytes = kStaticScratchBytes;
     return run_gemm<fp8bq::kModeWgrad>(dyqT, sdyT, xqT, sxT, o, N, K, M, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -27,7 +27,8 @@ BF16, F32 = 0, 1
 C_FUNCTIONS = (
     "fp8bq_quantize_rowwise", "fp8bq_quantize_colwise", "fp8bq_quantize_rowcol", "fp8bq_swiglu_quantize",
     "fp8bq_quantize_weight_block", "fp8bq_quantize_weight_blocks", "fp8bq_gemm_fprop", "fp8bq_gemm_fprop_q", "fp8bq_gemm_dgrad",
-    "fp8bq_gemm_wgrad", "fp8bq_gemm_wgrad_balanced", "fp8bq_gemm_wgrad_scratch_bytes", "fp8bq_gemm_wgrad_f32",
+    "fp8bq_gemm_wgrad", "fp8bq_gemm_wgrad_balanced", "fp8bq_gemm_wgrad_scratch_bytes",
+    "fp8bq_gemm_wgrad_balanced_static", "fp8bq_gemm_wgrad_f32",
     "fp8bq_mx_quantize_rowwise", "fp8bq_mx_quantize_colwise",
     "fp8bq_mx_quantize_rowcol", "fp8bq_mx_gemm", "fp8bq_check", "fp8bq_status_string", "fp8bq_selftest_wait_timeout",
 )
@@ -59,6 +60,7 @@ def _load():
         "fp8bq_gemm_wgrad": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
         "fp8bq_gemm_wgrad_balanced": [vp, vp, vp, vp, vp, i64, i64, i64, vp, i64, vp],
         "fp8bq_gemm_wgrad_scratch_bytes": [ctypes.POINTER(i64)],
+        "fp8bq_gemm_wgrad_balanced_static": [vp, vp, vp, vp, vp, i64, i64, i64, vp],
         "fp8bq_gemm_wgrad_f32": [vp, vp, vp, vp, vp, i64, i64, i64, i32, vp],
         "fp8bq_mx_quantize_rowwise": [vp, i32, i64, i64, i64, vp, vp, vp],
         "fp8bq_mx_quantize_colwise": [vp, i32, i64, i64, i64, vp, vp, vp],
@@ -319,6 +321,21 @@ def fp8bq_gemm_wgrad_balanced(dyqT, sdyT, xqT, sxT, dw, scratch) -> None:
         _raise(lib.fp8bq_gemm_wgrad_balanced(_ptr(dyqT), _ptr(sdyT), _ptr(xqT), _ptr(sxT), _ptr(dw), M, N, K,
                                              _ptr(scratch), scratch.numel(), _stream(dw)),
                "fp8bq_gemm_wgrad_balanced")
+
+
+def fp8bq_gemm_wgrad_balanced_static(dyqT, sdyT, xqT, sxT, dw) -> None:
+    """fp8bq_gemm_wgrad_balanced with the library's own scratch (no buffer argument); calls on one device
+    must be ordered on one stream."""
+    N, M = dyqT.shape
+    K = xqT.shape[0]
+    _need(dyqT, torch.uint8, (N, M), "dyqT")
+    _need(sdyT, torch.float32, (M // 128, N), "sdyT")
+    _need(xqT, torch.uint8, (K, M), "xqT")
+    _need(sxT, torch.float32, (M // 128, K), "sxT")
+    _need(dw, torch.bfloat16, (N, K), "dw")
+    with torch.cuda.device(dw.device):
+        _raise(lib.fp8bq_gemm_wgrad_balanced_static(_ptr(dyqT), _ptr(sdyT), _ptr(xqT), _ptr(sxT), _ptr(dw), M, N, K,
+                                                    _stream(dw)), "fp8bq_gemm_wgrad_balanced_static")
 
 
 def fp8bq_gemm_wgrad_f32(dyqT, sdyT, xqT, sxT, dw, accumulate: bool = False) -> None:

@@ -278,6 +278,22 @@ fp8bq_status fp8bq_gemm_wgrad_balanced(const uint8_t* dyqT, const float* sdyT, c
 fp8bq_status fp8bq_gemm_wgrad_scratch_bytes(int64_t* bytes);
 
 /*
+ * fp8bq_gemm_wgrad_balanced without a caller buffer: its scratch is a
+ * fixed array in the library's own device memory (allocated with the module,
+ * no allocation call), sized for up to 74 clusters (a 148-SM B300); a device
+ * that runs more clusters gets FP8BQ_ERR_SHAPE.  The same result, bit for
+ * bit, as fp8bq_gemm_wgrad_balanced.  Calls on one device must not overlap in
+ * time (they share the array: order them on one stream).  After
+ * FP8BQ_ERR_TIMEOUT the array's counters may be left non-zero; reload the
+ * library.  Other arguments as fp8bq_gemm_wgrad.
+ * Source: the pages have no counterpart (an allocation-free form of the
+ *   balanced Wgrad above).
+ */
+fp8bq_status fp8bq_gemm_wgrad_balanced_static(const uint8_t* dyqT, const float* sdyT, const uint8_t* xqT,
+                                              const float* sxT, uint16_t* dw, int64_t M, int64_t N, int64_t K,
+                                              fp8bq_stream_t stream);
+
+/*
  * Wgrad with an FP32 output, for keeping weight gradients in FP32 across
  * micro-batches and data-parallel ranks (the Puro-2B report keeps training
  * state in FP32, section 2 "FP8").  Same operands and product as

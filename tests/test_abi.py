@@ -134,6 +134,9 @@ def test_fused_and_fp32_entry_points_reject_bad_arguments_on_the_host(lib):
     assert wb(P, P, P, P, P, 128, 128, 128, P, -1, None) == ERR_SHAPE
     assert wb(P, P, P, P, P, 100, 128, 128, P, 1 << 30, None) == ERR_SHAPE      # M not a multiple of 128
     assert wb(P, P, P, P, None, 128, 128, 128, P, 1 << 30, None) == ERR_NULL
+    ws = lib.fp8bq_gemm_wgrad_balanced_static
+    ws.restype, ws.argtypes = i32, [vp] * 5 + [i64] * 3 + [vp]
+    assert ws(P, P, P, P, None, 128, 128, 128, None) == ERR_NULL
     sb = lib.fp8bq_gemm_wgrad_scratch_bytes
     sb.restype, sb.argtypes = i32, [vp]
     assert sb(None) == ERR_NULL
