@@ -30,8 +30,8 @@ __device__ unsigned int g_status_taken;
 // counters zero again.
 constexpr int kStaticScratchPairs = 74;
 constexpr int64_t kStaticScratchBytes =
-    ((static_cast<int64_t>(kStaticScratchPairs - 1) * fp8bq::kSplitBoundaryCounters * 4 + 255) / 256) * 256 +
-    static_cast<int64_t>(kStaticScratchPairs - 1) * fp8bq::kSplitBoundaryBytes;
+    ((static_cast<int64_t>(kStaticScratchPairs - 1) * fp8bq::kSplitTileCounters * 4 + 255) / 256) * 256 +
+    static_cast<int64_t>(kStaticScratchPairs) * fp8bq::kSplitClusterBytes;
 static __device__ __align__(256) uint8_t g_wgrad_scratch[kStaticScratchBytes];
 
 // Reads the status word and clears it in one atomic step, so a timeout that
@@ -288,13 +288,13 @@ struct GemmOut {
 };
 
 // Scratch of the balanced order for `pairs` clusters: one arrival counter per
-// boundary, CTA rank and promotion warp (rounded up to 256 bytes), then the
-// boundaries' split slots.
+// remaining tile (at most pairs - 1 of them), CTA rank and promotion warp
+// (rounded up to 256 bytes), then each cluster's two split slots.
 int64_t split_counter_bytes(int pairs) {
-    return ((static_cast<int64_t>(pairs - 1) * fp8bq::kSplitBoundaryCounters * 4 + 255) / 256) * 256;
+    return ((static_cast<int64_t>(pairs - 1) * fp8bq::kSplitTileCounters * 4 + 255) / 256) * 256;
 }
 int64_t split_scratch_bytes(int pairs) {
-    return pairs < 2 ? 0 : split_counter_bytes(pairs) + static_cast<int64_t>(pairs - 1) * fp8bq::kSplitBoundaryBytes;
+    return pairs < 2 ? 0 : split_counter_bytes(pairs) + static_cast<int64_t>(pairs) * fp8bq::kSplitClusterBytes;
 }
 
 // n FP32 values set to v (scales of all-zero tiles).
@@ -396,19 +396,16 @@ fp8bq_status run_gemm(const uint8_t* A, const float* sA, const uint8_t* B, const
     p.timeout_ns = kDefaultTimeoutNs;
     // persistent: one CTA pair per TPC that can hold one, never more pairs than tiles
     const int pairs = static_cast<int>(tiles < dev->max_pairs ? tiles : dev->max_pairs);
-    // balanced order (with scratch): every cluster gets an equal share of the
-    // chunks; it needs at least one whole tile per cluster (tiles >= pairs,
-    // always true here) and two clusters to share anything
+    // balanced order (with scratch, Wgrad only): the whole-tile rounds run in
+    // tile order and the chunks of the tiles left over for a last, partly
+    // filled round are shared out equally between all clusters.  Used where
+    // that round would leave at least 10 % of the clusters idle; its
+    // remainder chunk arithmetic is 32-bit.
     p.split_ws = nullptr;
     p.split_cnt = nullptr;
-    // balanced order: only Wgrad offers it, its chunk count must fit the
-    // kernel's 32-bit share arithmetic, and it is used where whole-tile rounds
-    // would leave at least 10 % of the clusters' time idle in the last round
-    // (it costs about 5 % per chunk: the clusters no longer walk their tiles
-    // in step, so concurrent tiles share fewer operand chunks in L2)
-    const int64_t rounds = (tiles + pairs - 1) / pairs;
-    const bool balanced = MODE == fp8bq::kModeWgrad && o.scratch != nullptr && pairs >= 2 &&
-                          tiles * p.KC < (int64_t(1) << 31) && 10 * (rounds * pairs - tiles) >= rounds * pairs;
+    const int64_t rem = tiles % pairs;
+    const bool balanced = MODE == fp8bq::kModeWgrad && o.scratch != nullptr && pairs >= 2 && rem > 0 &&
+                          10 * rem <= 9 * static_cast<int64_t>(pairs) && rem * p.KC * pairs < (int64_t(1) << 31);
     if (balanced) {
         p.split_cnt = reinterpret_cast<unsigned int*>(o.scratch);
         p.split_ws = reinterpret_cast<float*>(o.scratch + split_counter_bytes(pairs));

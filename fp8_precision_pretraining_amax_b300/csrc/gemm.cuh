@@ -81,11 +81,11 @@ constexpr uint32_t kStageBytesA = kBM * kBK;
 constexpr uint32_t kStageBytesB = kBNHalf * kBK;
 constexpr uint32_t kTmemCols = 2 * kBN;
 // Balanced order: one promotion warp's accumulators (32 threads x 128 floats)
-// in a split slot, and the slots' and counters' sizes per boundary between
-// two clusters (2 parts x 2 CTA ranks x 8 warps).
+// in a split slot; the slots of one cluster (2 remainder segments x 2 CTA
+// ranks x 8 warps) and the counters of one remaining tile (2 ranks x 8 warps).
 constexpr int64_t kSplitSliceFloats = 32 * 128;
-constexpr int64_t kSplitBoundaryBytes = 2 * 2 * kPromoWarps * kSplitSliceFloats * 4;
-constexpr int64_t kSplitBoundaryCounters = 2 * kPromoWarps;
+constexpr int64_t kSplitClusterBytes = 2 * 2 * kPromoWarps * kSplitSliceFloats * 4;
+constexpr int64_t kSplitTileCounters = 2 * kPromoWarps;
 // Epilogue staging: a promotion warp writes its 32 rows x 128 BF16 columns
 // as four 32 x 32 boxes (64-byte rows, 64-byte swizzle) through three 2 KB
 // staging boxes used in rotation, so a box is written while the TMA stores
@@ -167,44 +167,54 @@ __device__ __forceinline__ bool warp_wait_backoff(uint64_t* bar, uint32_t parity
 // the same bound (any order of the FP32 sum over chunks is a valid reading).
 __device__ __forceinline__ int chunk_of(int i, int it, int KC) { return (it & 1) ? KC - 1 - i : i; }
 
-// Balanced order (the kBal kernels, Wgrad with scratch): cluster cid of n
-// takes the equal share [U cid / n, U (cid + 1) / n) of all U = num_tiles *
-// KC chunks in tile-major order (U < 2^31), so no cluster idles in a last,
-// partly filled wave of long tiles.  With num_tiles >= n every share holds
-// at least one tile's worth of chunks, so a tile is split between at most two
-// neighbouring clusters: its first chunks end cluster b's share ("part 0"),
-// the rest begin cluster b + 1's ("part 1"); b names the split.
-struct BalIter {
-    int u, u_end;
-};
-
-__device__ __forceinline__ BalIter bal_init(const GemmParams& p, int cid, int ncl) {
-    const int64_t U = static_cast<int64_t>(p.num_tiles) * p.KC;
-    return BalIter{static_cast<int>(U * cid / ncl), static_cast<int>(U * (cid + 1) / ncl)};
+// Balanced order (the kBal kernels, Wgrad with scratch).  Whole-tile rounds
+// leave the grid partly idle in the last round when num_tiles is not a
+// multiple of the n clusters, and a Wgrad tile reduces over all tokens, so
+// that round costs a whole tile's time.  Here the R = num_tiles / n full
+// rounds run in tile order (cluster cid: tiles cid, cid + n, ..., walking
+// odd rounds backwards, so concurrent tiles share operand chunks in L2), and
+// the chunks of the rem = num_tiles - R n remaining tiles, U_r = rem * KC in
+// tile-major order, are shared out equally: cluster c takes [b_c, b_{c+1}),
+// b_c = U_r c / n.  A share is no longer than a tile, so it lies in at most
+// two remaining tiles (the cluster's remainder segments 0 and 1), and a
+// remaining tile is covered by every cluster whose share meets it: its parts.
+// The host guarantees U_r * n < 2^31.
+__device__ __forceinline__ int rem_bound(const GemmParams& p, int ncl, int c) {
+    const int rem = p.num_tiles - (p.num_tiles / ncl) * ncl;
+    return rem * p.KC * c / ncl;
 }
 
-// The next segment of the share: chunks [c_lo, c_hi) of tile; false at its end.
-__device__ __forceinline__ bool bal_next(BalIter& b, const GemmParams& p, int& tile, int& c_lo, int& c_hi) {
-    if (b.u >= b.u_end) return false;
-    tile = b.u / p.KC;
-    c_lo = b.u - tile * p.KC;
-    c_hi = min(p.KC, c_lo + (b.u_end - b.u));
-    b.u += c_hi - c_lo;
-    return true;
-}
-
-// Segment k of cluster cid's balanced share, recomputed from scratch (no
-// state carried between segments): false when the share has no segment k.
-__device__ __forceinline__ bool bal_segment(const GemmParams& p, int cid, int ncl, int k, int& tile, int& c_lo,
-                                            int& c_hi) {
-    const BalIter b = bal_init(p, cid, ncl);
-    const int t = b.u / p.KC + k;
-    const int lo = max(b.u, t * p.KC), hi = min(b.u_end, (t + 1) * p.KC);
+// Segment k of cluster cid: chunks [c_lo, c_hi) of tile; rt = the remaining
+// tile's index (-1 in the full rounds).  False when there is no segment k.
+__device__ __forceinline__ bool hyb_segment(const GemmParams& p, int cid, int ncl, int k, int& tile, int& c_lo,
+                                            int& c_hi, int& rt) {
+    const int R = p.num_tiles / ncl;
+    if (k < R) {
+        tile = cid + k * ncl;
+        c_lo = 0;
+        c_hi = p.KC;
+        rt = -1;
+        return true;
+    }
+    const int b0 = rem_bound(p, ncl, cid), b1 = rem_bound(p, ncl, cid + 1);
+    const int t = b0 / p.KC + (k - R);
+    const int lo = max(b0, t * p.KC), hi = min(b1, (t + 1) * p.KC);
     if (lo >= hi) return false;
-    tile = t;
+    rt = t;
+    tile = R * ncl + t;
     c_lo = lo - t * p.KC;
     c_hi = hi - t * p.KC;
     return true;
+}
+
+// All chunks cluster cid works through in the balanced order.
+__device__ __forceinline__ int hyb_chunk_count(const GemmParams& p, int cid, int ncl) {
+    return (p.num_tiles / ncl) * p.KC + rem_bound(p, ncl, cid + 1) - rem_bound(p, ncl, cid);
+}
+
+// Does cluster c's share meet remaining tile rt?
+__device__ __forceinline__ bool hyb_meets(const GemmParams& p, int ncl, int c, int rt) {
+    return max(rem_bound(p, ncl, c), rt * p.KC) < min(rem_bound(p, ncl, c + 1), (rt + 1) * p.KC);
 }
 
 // Stop both CTAs of the pair and record the timeout.
@@ -306,11 +316,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t full0 = mapa_shared(smem_addr(&ctl->full[0]), 0);
         uint32_t s = 0, ph = 0, issued = 0;
         bool ok = true;
-        int it = -1, tile = first_tile - tile_step, c_lo = 0, c_hi = p.KC;
-        BalIter bi = bal_init(p, first_tile, tile_step);
+        int it = -1, tile = first_tile - tile_step, c_lo = 0, c_hi = p.KC, rt = -1;
         while (ok) {
             if constexpr (kBal) {
-                if (!bal_next(bi, p, tile, c_lo, c_hi)) break;
+                if (!hyb_segment(p, first_tile, tile_step, it + 1, tile, c_lo, c_hi, rt)) break;
             } else {
                 tile += tile_step;
                 if (tile >= p.num_tiles) break;
@@ -320,7 +329,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int r0 = tm * kPairM + static_cast<int>(rank) * kBM;  // this CTA's first row
             const int b0 = tn * kBN + static_cast<int>(rank) * kBNHalf;  // this CTA's first B row
             for (int i = c_lo; i < c_hi; ++i) {
-                const int c = kBal ? i : chunk_of(i, it, p.KC);
+                const int c = rt >= 0 ? i : chunk_of(i, it, p.KC);
                 if (!warp_wait(&ctl->empty[s], ph ^ 1, abort_flag, lim)) { ok = false; break; }
                 if (lane == 0) {
                     if (leader) mbar_arrive_expect_tx(&ctl->full[s], 2 * (kStageBytesA + kStageBytesB));
@@ -343,11 +352,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // the problem are skipped.
         uint32_t q = 0, qph = 0, issued = 0;
         bool ok = true;
-        int it = -1, tile = first_tile - tile_step, c_lo = 0, c_hi = p.KC;
-        BalIter bi = bal_init(p, first_tile, tile_step);
+        int it = -1, tile = first_tile - tile_step, c_lo = 0, c_hi = p.KC, rt = -1;
         while (ok) {
             if constexpr (kBal) {
-                if (!bal_next(bi, p, tile, c_lo, c_hi)) break;
+                if (!hyb_segment(p, first_tile, tile_step, it + 1, tile, c_lo, c_hi, rt)) break;
             } else {
                 tile += tile_step;
                 if (tile >= p.num_tiles) break;
@@ -359,7 +367,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint32_t a_bytes = r0 < p.I ? 128u * 4u : 0u;
             const uint32_t b_bytes = MODE == kModeWgrad ? static_cast<uint32_t>(min(p.J - j0, kBN)) * 4u : 0u;
             for (int i = c_lo; i < c_hi; ++i) {
-                const int c = kBal ? i : chunk_of(i, it, p.KC);
+                const int c = rt >= 0 ? i : chunk_of(i, it, p.KC);
                 if (!warp_wait_backoff(&ctl->sempty[q], qph ^ 1, abort_flag, lim)) { ok = false; break; }
                 ScaleSlot& sl = ctl->scl[q];
                 if (lane == 0) {
@@ -392,9 +400,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             constexpr uint32_t idesc = idesc_e4m3_f32(kPairM, kBN);
             uint32_t s = 0, ph = 0, buf = 0, tph = 0;
             // balanced: the MMAs need no tile boundaries, one flat loop
-            const BalIter bi = bal_init(p, first_tile, tile_step);
             const int n_outer = kBal ? 1 : p.num_tiles;
-            const int n_inner = kBal ? bi.u_end - bi.u : p.KC;
+            const int n_inner = kBal ? hyb_chunk_count(p, first_tile, tile_step) : p.KC;
             for (int tile = kBal ? 0 : first_tile; tile < n_outer && ok; tile += kBal ? 1 : tile_step) {
                 for (int c = 0; c < n_inner; ++c) {
                     // Both waits suspend (try_wait): this thread shares its SM
@@ -437,10 +444,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         uint32_t buf = 0, tph = 0, q = 0, qph = 0;
         int nbox = 0;   // staging box of the next BF16 output box
         bool ok = true;
-        int tile = first_tile - tile_step, c_lo = 0, c_hi = p.KC;
+        int tile = first_tile - tile_step, c_lo = 0, c_hi = p.KC, rt = -1;
         for (int seg = 0; ok; ++seg) {
             if constexpr (kBal) {
-                if (!bal_segment(p, first_tile, tile_step, seg, tile, c_lo, c_hi)) break;
+                if (!hyb_segment(p, first_tile, tile_step, seg, tile, c_lo, c_hi, rt)) break;
             } else {
                 tile += tile_step;
                 if (tile >= p.num_tiles) break;
@@ -541,39 +548,53 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             if (!ok) break;
             if constexpr (kBal) {
-                if (c_lo > 0 || c_hi < p.KC) {
-                    // A tile split between two clusters (see BalIter): each part
-                    // leaves its partial accumulators in the split slot of its
-                    // boundary, then counts itself in; the part that arrives
-                    // second adds the other's partial to its own (FP32 addition
-                    // commutes: the sum does not depend on the order of
-                    // arrival) and writes the tile.  Warp-sized slices: warp pw
-                    // of either part holds the same rows and columns.
-                    const int part = c_lo == 0 ? 0 : 1;
-                    const int bnd = part == 0 ? first_tile : first_tile - 1;
-                    float* mine = p.split_ws +
-                                  ((static_cast<int64_t>(bnd) * 2 + part) * 2 + rank) * kSplitSliceFloats * kPromoWarps +
-                                  static_cast<int64_t>(pw) * kSplitSliceFloats;
-                    const float* other = mine + (part == 0 ? 2 : -2) * kSplitSliceFloats * kPromoWarps;
+                if (rt >= 0) {
+                    // A remaining tile, shared by the clusters whose shares meet
+                    // it (see hyb_segment).  Each part leaves its partial
+                    // accumulators in its own slot (cluster, segment) and counts
+                    // itself in; the last to arrive sums every part's slot in
+                    // cluster order (the same sum whichever part arrives last)
+                    // and writes the tile.  Warp-sized slices: warp pw of every
+                    // part holds the same rows and columns.
+                    const int ncl = tile_step;
+                    const int ur = (p.num_tiles - (p.num_tiles / ncl) * ncl) * p.KC;
+                    const int cf =
+                        min(ncl - 1, static_cast<int>(((static_cast<int64_t>(rt) * p.KC + 1) * ncl - 1) / ur));
+                    const int cl = min(ncl - 1, static_cast<int>((static_cast<int64_t>(rt + 1) * p.KC * ncl - 1) / ur));
+                    auto slot = [&](int c) -> float* {
+                        const int j = rem_bound(p, ncl, c) / p.KC == rt ? 0 : 1;
+                        return p.split_ws +
+                               ((static_cast<int64_t>(c) * 2 + j) * 2 + rank) * kSplitSliceFloats * kPromoWarps +
+                               static_cast<int64_t>(pw) * kSplitSliceFloats;
+                    };
+                    float* mine = slot(first_tile);
 #pragma unroll
                     for (int i4 = 0; i4 < 32; ++i4)
                         *reinterpret_cast<float4*>(mine + (i4 * 32 + lane) * 4) =
                             make_float4(acc[4 * i4], acc[4 * i4 + 1], acc[4 * i4 + 2], acc[4 * i4 + 3]);
                     __threadfence();
                     __syncwarp();
-                    unsigned int* cnt = p.split_cnt + (bnd * 2 + static_cast<int>(rank)) * kPromoWarps + pw;
+                    unsigned int nparts = 0;
+                    for (int c = cf; c <= cl; ++c) nparts += hyb_meets(p, ncl, c, rt) ? 1u : 0u;
+                    unsigned int* cnt = p.split_cnt + (rt * 2 + static_cast<int>(rank)) * kPromoWarps + pw;
                     unsigned int arrived = 0;
                     if (lane == 0) arrived = atomicAdd(cnt, 1u);
                     arrived = __shfl_sync(0xFFFFFFFFu, arrived, 0);
-                    if (arrived == 0) continue;   // the other part completes the tile
+                    if (arrived + 1 != nparts) continue;   // another part completes the tile
                     __threadfence();
 #pragma unroll
-                    for (int i4 = 0; i4 < 32; ++i4) {
-                        const float4 o = __ldcg(reinterpret_cast<const float4*>(other + (i4 * 32 + lane) * 4));
-                        acc[4 * i4] = __fadd_rn(acc[4 * i4], o.x);
-                        acc[4 * i4 + 1] = __fadd_rn(acc[4 * i4 + 1], o.y);
-                        acc[4 * i4 + 2] = __fadd_rn(acc[4 * i4 + 2], o.z);
-                        acc[4 * i4 + 3] = __fadd_rn(acc[4 * i4 + 3], o.w);
+                    for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+                    for (int c = cf; c <= cl; ++c) {
+                        if (!hyb_meets(p, ncl, c, rt)) continue;
+                        const float* part = slot(c);
+#pragma unroll
+                        for (int i4 = 0; i4 < 32; ++i4) {
+                            const float4 o = __ldcg(reinterpret_cast<const float4*>(part + (i4 * 32 + lane) * 4));
+                            acc[4 * i4] = __fadd_rn(acc[4 * i4], o.x);
+                            acc[4 * i4 + 1] = __fadd_rn(acc[4 * i4 + 1], o.y);
+                            acc[4 * i4 + 2] = __fadd_rn(acc[4 * i4 + 2], o.z);
+                            acc[4 * i4 + 3] = __fadd_rn(acc[4 * i4 + 3], o.w);
+                        }
                     }
                     if (lane == 0) *cnt = 0u;   // zero again for the next launch
                 }

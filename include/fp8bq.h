@@ -243,19 +243,19 @@ fp8bq_status fp8bq_gemm_wgrad(const uint8_t* dyqT, const float* sdyT, const uint
                               uint16_t* dw, int64_t M, int64_t N, int64_t K, fp8bq_stream_t stream);
 
 /*
- * Wgrad, balanced work split: the same product as fp8bq_gemm_wgrad, with
- * every cluster of the persistent grid taking an equal share of all tiles'
- * reduction chunks instead of whole tiles, so no cluster idles in a last,
- * partly filled wave of tiles (each Wgrad tile reduces over all M tokens, so
- * such a wave costs a whole tile's time).  The split is used where whole-tile
- * rounds would leave at least 10 % of the grid's time idle; otherwise the
- * call runs fp8bq_gemm_wgrad's tile order (scratch untouched).  A tile split between two
- * neighbouring clusters is completed by the one that finishes second: it
- * adds the other's FP32 partial, left in `scratch`, to its own (FP32
- * addition commutes, so the result does not depend on which finishes first
- * and is the same on every call).  The result differs from
- * fp8bq_gemm_wgrad's only in the grouping of the FP32 sum over chunks on
- * split tiles: within the same acceptance bound.
+ * Wgrad, balanced work split: the same product as fp8bq_gemm_wgrad.  The
+ * persistent grid's whole-tile rounds run in fp8bq_gemm_wgrad's tile order;
+ * the reduction chunks of the tiles left over for a last, partly filled
+ * round are shared out equally between all clusters, so no cluster idles
+ * through that round (each Wgrad tile reduces over all M tokens, so it costs
+ * a whole tile's time).  The split is used where that round would leave at
+ * least 10 % of the clusters idle; otherwise the call runs fp8bq_gemm_wgrad's
+ * tile order (scratch untouched).  Each cluster leaves its FP32 partial of a
+ * shared tile in `scratch`; the last to finish adds all the parts in cluster
+ * order and writes the tile, so the result does not depend on which finishes
+ * last and is the same on every call.  It differs from fp8bq_gemm_wgrad's
+ * only in the grouping of the FP32 sum over chunks on the shared tiles:
+ * within the same acceptance bound.
  *   scratch        device buffer of at least scratch_bytes bytes, 16-byte
  *                  aligned, all zero before its first use; every completed
  *                  call leaves it ready for the next (the arrival counters at

@@ -307,17 +307,19 @@ def test_fprop_q_empty_reduction(fb):
 def _split_counter_bytes(fb):
     """Bytes of the balanced Wgrad's arrival counters at the start of its
     scratch (one 4-byte counter per CTA rank and promotion warp, 16 per
-    boundary between two clusters; each boundary also has 512 KB of slots)."""
+    remaining tile, rounded up to 256 bytes); then each cluster's 512 KB of
+    split slots."""
     total = fb.fp8bq_gemm_wgrad_scratch_bytes()
-    return (total // (512 * 1024 + 64)) * 64
+    return total - (total // (512 * 1024)) * (512 * 1024)
 
 
 def test_wgrad_balanced_splits_tiles_and_repeats_bit_for_bit(fb):
     """81 output tiles of 256 x 256, 16 chunks each, over the persistent
-    grid's clusters: most clusters' equal shares of the chunks end inside a
-    tile, which the two neighbours then complete together.  Every output
-    tile is within the bound, a second call gives the same bits, and the
-    arrival counters are back at zero."""
+    grid's clusters: one whole-tile round, then the chunks of the tiles left
+    over shared out between all clusters, so that several clusters complete
+    each of those tiles together.  Every output tile is within the bound, a
+    second call gives the same bits, and the arrival counters are back at
+    zero."""
     rng = np.random.default_rng(29)
     M, N, K = 2048, 2304, 2304
     dyqT, xqT = random_codes(rng, (N, M)), random_codes(rng, (K, M))
@@ -334,6 +336,41 @@ def test_wgrad_balanced_splits_tiles_and_repeats_bit_for_bit(fb):
     nc = _split_counter_bytes(fb)
     assert nc > 0 and int(scratch[:nc].sum()) == 0
     check_gemm_tiles(dw1, oracle.gemm_wgrad_mm, (dyqT, sdyT, xqT, sxT), _all_tiles(N, K), what="wgrad balanced")
+
+
+def test_wgrad_balanced_one_leftover_tile_many_parts(fb):
+    """75 output tiles on at most 74 clusters, 32 chunks each: the whole-tile
+    round matches fp8bq_gemm_wgrad bit for bit (same tiles, same chunk order),
+    and the one tile left over is shared by up to 32 clusters, one chunk
+    each, while the rest have empty shares; it is within the bound, the same
+    on a second call, and the counters are back at zero."""
+    rng = np.random.default_rng(41)
+    M, N, K = 4096, 768, 6400
+    dyqT, xqT = random_codes(rng, (N, M)), random_codes(rng, (K, M))
+    sdyT, sxT = random_scales(rng, (M // 128, N)), random_scales(rng, (M // 128, K))
+    dev = [to_dev(a) for a in (dyqT, sdyT, xqT, sxT)]
+    scratch = fb.wgrad_scratch(dev[0].device)
+    dw1 = torch.empty((N, K), dtype=torch.bfloat16, device="cuda")
+    dw2 = torch.empty_like(dw1)
+    fb.fp8bq_gemm_wgrad_balanced(*dev, dw1, scratch)
+    fb.fp8bq_gemm_wgrad_balanced(*dev, dw2, scratch)
+    ref = fb.gemm_wgrad(*dev)
+    fb.check()
+    torch.cuda.synchronize()
+    assert torch.equal(dw1.view(torch.int16), dw2.view(torch.int16))
+    nc = _split_counter_bytes(fb)
+    assert int(scratch[:nc].sum()) == 0
+    # one cluster per two SMs (74 on a 148-SM B300): the tiles left over for
+    # the last round are the last tiles in row-major order
+    pairs = min(75, torch.cuda.get_device_properties(0).multi_processor_count // 2)
+    last = (N // 256 - 1, K // 256 - 1)
+    same = torch.ones(75, dtype=torch.bool)
+    same[75 - 75 % pairs:] = False
+    same = same.view(N // 256, K // 256)
+    eq = (dw1.view(torch.int16) == ref.view(torch.int16)).view(N // 256, 256, K // 256, 256).all(3).all(1).cpu()
+    assert bool(eq[same].all())
+    picks = [(2 * last[0] + a, 2 * last[1] + b) for a in (0, 1) for b in (0, 1)] + [(0, 0), (3, 20)]
+    check_gemm_tiles(dw1, oracle.gemm_wgrad_mm, (dyqT, sdyT, xqT, sxT), picks, what="wgrad balanced leftover")
 
 
 def test_wgrad_balanced_exact_integer_case_is_bit_exact(fb):
