@@ -107,7 +107,7 @@ struct GemmParams {
     int out_q;            // also quantize the BF16-rounded output per 1x128 row tile
     float* sq;            // out_q: output scales [J/128][I]
     float* split_ws;      // balanced order: partial accumulators of split tiles
-    unsigned int* split_cnt;  // balanced order: arrival counters (boundary, CTA rank, warp)
+    unsigned int* split_cnt;  // balanced order: arrival counters (remaining tile, CTA rank, warp)
     uint64_t timeout_ns;
 };
 
@@ -165,7 +165,7 @@ __device__ __forceinline__ bool warp_wait_backoff(uint64_t* bar, uint32_t parity
 // that wave (the B column blocks of a row-major wave) come from L2 instead of
 // HBM.  Chunk partials are summed in that order; the result stays within
 // the same bound (any order of the FP32 sum over chunks is a valid reading).
-__device__ __forceinline__ int chunk_of(int i, int it, int KC) { return (it & 1) ? KC - 1 - i : i; }
+__host__ __device__ __forceinline__ int chunk_of(int i, int it, int KC) { return (it & 1) ? KC - 1 - i : i; }
 
 // Balanced order (the kBal kernels, Wgrad with scratch).  Whole-tile rounds
 // leave the grid partly idle in the last round when num_tiles is not a
@@ -179,15 +179,15 @@ __device__ __forceinline__ int chunk_of(int i, int it, int KC) { return (it & 1)
 // two remaining tiles (the cluster's remainder segments 0 and 1), and a
 // remaining tile is covered by every cluster whose share meets it: its parts.
 // The host guarantees U_r * n < 2^31.
-__device__ __forceinline__ int rem_bound(const GemmParams& p, int ncl, int c) {
+__host__ __device__ __forceinline__ int rem_bound(const GemmParams& p, int ncl, int c) {
     const int rem = p.num_tiles - (p.num_tiles / ncl) * ncl;
     return rem * p.KC * c / ncl;
 }
 
 // Segment k of cluster cid: chunks [c_lo, c_hi) of tile; rt = the remaining
 // tile's index (-1 in the full rounds).  False when there is no segment k.
-__device__ __forceinline__ bool hyb_segment(const GemmParams& p, int cid, int ncl, int k, int& tile, int& c_lo,
-                                            int& c_hi, int& rt) {
+__host__ __device__ __forceinline__ bool hyb_segment(const GemmParams& p, int cid, int ncl, int k, int& tile,
+                                                     int& c_lo, int& c_hi, int& rt) {
     const int R = p.num_tiles / ncl;
     if (k < R) {
         tile = cid + k * ncl;
@@ -208,13 +208,28 @@ __device__ __forceinline__ bool hyb_segment(const GemmParams& p, int cid, int nc
 }
 
 // All chunks cluster cid works through in the balanced order.
-__device__ __forceinline__ int hyb_chunk_count(const GemmParams& p, int cid, int ncl) {
+__host__ __device__ __forceinline__ int hyb_chunk_count(const GemmParams& p, int cid, int ncl) {
     return (p.num_tiles / ncl) * p.KC + rem_bound(p, ncl, cid + 1) - rem_bound(p, ncl, cid);
 }
 
 // Does cluster c's share meet remaining tile rt?
-__device__ __forceinline__ bool hyb_meets(const GemmParams& p, int ncl, int c, int rt) {
+__host__ __device__ __forceinline__ bool hyb_meets(const GemmParams& p, int ncl, int c, int rt) {
     return max(rem_bound(p, ncl, c), rt * p.KC) < min(rem_bound(p, ncl, c + 1), (rt + 1) * p.KC);
+}
+
+// The clusters that can hold a part of remaining tile rt: [first, last], the
+// clusters whose shares start at or before its first and last chunks (an
+// empty share in between meets no tile: check each with hyb_meets).
+__host__ __device__ __forceinline__ void hyb_part_range(const GemmParams& p, int ncl, int rt, int& first, int& last) {
+    const int64_t ur = static_cast<int64_t>(p.num_tiles - (p.num_tiles / ncl) * ncl) * p.KC;
+    first = min(ncl - 1, static_cast<int>(((static_cast<int64_t>(rt) * p.KC + 1) * ncl - 1) / ur));
+    last = min(ncl - 1, static_cast<int>((static_cast<int64_t>(rt + 1) * p.KC * ncl - 1) / ur));
+}
+
+// Which of cluster c's remainder segments (0 or 1) covers remaining tile rt:
+// its split slot.
+__host__ __device__ __forceinline__ int hyb_slot_segment(const GemmParams& p, int ncl, int c, int rt) {
+    return rem_bound(p, ncl, c) / p.KC == rt ? 0 : 1;
 }
 
 // Stop both CTAs of the pair and record the timeout.
@@ -557,12 +572,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     // and writes the tile.  Warp-sized slices: warp pw of every
                     // part holds the same rows and columns.
                     const int ncl = tile_step;
-                    const int ur = (p.num_tiles - (p.num_tiles / ncl) * ncl) * p.KC;
-                    const int cf =
-                        min(ncl - 1, static_cast<int>(((static_cast<int64_t>(rt) * p.KC + 1) * ncl - 1) / ur));
-                    const int cl = min(ncl - 1, static_cast<int>((static_cast<int64_t>(rt + 1) * p.KC * ncl - 1) / ur));
+                    int cf, cl;
+                    hyb_part_range(p, ncl, rt, cf, cl);
                     auto slot = [&](int c) -> float* {
-                        const int j = rem_bound(p, ncl, c) / p.KC == rt ? 0 : 1;
+                        const int j = hyb_slot_segment(p, ncl, c, rt);
                         return p.split_ws +
                                ((static_cast<int64_t>(c) * 2 + j) * 2 + rank) * kSplitSliceFloats * kPromoWarps +
                                static_cast<int64_t>(pw) * kSplitSliceFloats;
